@@ -1,0 +1,388 @@
+"""Benchmark of the paged-KV decode hot path on GB300.
+
+A step is one pass of the hot path over one batch of the Llama-3-8B-shaped
+decode layer: kv_append of the batch's 64 new tokens, then paged_decode of the
+64 queries over their paged contexts (split-KV partitions + LSE combine).
+Inputs are seeded synthetic tensors already resident in HBM.  Prints ONE JSON
+line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only baseline that exists for
+this path) on the host cores, on a bounded sample of the same workload.
+Multi-GPU runs are independent replicas (the decode batch does not exchange
+data), reported as weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode HBM GB/s (% of ~8 TB/s peak) and decode tokens/s per layer"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = "8b"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--min-warm-seconds", type=float, default=1.0,
+                   help="warm-up also runs at least this long (clock sampling under load)")
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the GPU works."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def kernel_traffic(kernel_src: str, summary: str):
+    """DRAM bytes per launch recorded by an ncu capture of this exact kernel source."""
+    try:
+        digest = hashlib.sha1(open(kernel_src, "rb").read()).hexdigest()[:12]
+        text = open(summary).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)\s*\(source sha1 ([0-9a-f]+)",
+                  text)
+    if m and m.group(2) == digest:
+        return float(m.group(1))
+    return None
+
+
+def workload_bytes(case):
+    """Algorithmic bytes of one step: decode reads every attended K/V row once, q,
+    block-table entries and context lengths once, writes out once; kv_append reads
+    the new rows and writes them into the pool."""
+    import torch
+    S, Hq, D = case.q.shape
+    Hkv = case.k_pool.shape[1]
+    esz = case.q.element_size()
+    lens = case.context_lens.cpu().to(torch.int64)
+    tokens = int(lens.sum())
+    kv = tokens * Hkv * D * esz * 2
+    nblk = int(((lens + 15) // 16).sum())
+    decode = kv + 2 * S * Hq * D * esz + nblk * 4 + S * 4
+    T = case.k_new.shape[0]
+    append = 2 * 2 * T * Hkv * D * esz + T * 8
+    return decode, append, tokens
+
+
+def run_reference(args, ws, rank):
+    """fp64 CPU oracle on the host cores: each step is a bounded sample of the batch."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import synth
+    oracle.build()
+    case = synth.build_case(WORKLOAD, "cpu")
+    decode_bytes, append_bytes, tokens = workload_bytes(case)
+    kp, vp = synth.host_bits(case.k_pool), synth.host_bits(case.v_pool)
+    q, bt = synth.host_bits(case.q), synth.host_bits(case.block_tables)
+    cl = synth.host_bits(case.context_lens)
+    slots, kn, vn = (synth.host_bits(case.slot_mapping), synth.host_bits(case.k_new),
+                     synth.host_bits(case.v_new))
+    oracle.kv_append(slots, kn, vn, kp, vp)
+    S = q.shape[0]
+    # calibrate one full pass, then size each step's sample so the run stays bounded
+    t0 = time.perf_counter()
+    oracle.paged_decode(q, kp, vp, bt, cl, case.scale)
+    t_full = time.perf_counter() - t0
+    budget = 150.0
+    n = max(1, min(S, int(S * budget / max(1e-9, (args.steps + args.warmup) * t_full))))
+    idx = np.arange(n)
+    sub_bytes = decode_bytes * float(cl[idx].astype(np.int64).sum()) / tokens
+    for _ in range(args.warmup):
+        oracle.paged_decode(q[idx], kp, vp, bt[idx], cl[idx], case.scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.paged_decode(q[idx], kp, vp, bt[idx], cl[idx], case.scale)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = sub_bytes / dt / 1e9
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "tokens_per_s_per_layer": n / dt,
+        "config": {"workload": case.wl.name, "num_seqs": S, "sample_seqs": n},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} of {S} sequences per step (all heads), "
+                                   f"full pass {t_full:.3f} s"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(case, decode_bytes, tokens):
+    """The oracle as it stands, on the host cores, over repeated full passes (~5 s)."""
+    import oracle
+    import synth
+    oracle.build()
+    kp, vp = synth.host_bits(case.k_pool), synth.host_bits(case.v_pool)
+    oracle.kv_append(synth.host_bits(case.slot_mapping), synth.host_bits(case.k_new),
+                     synth.host_bits(case.v_new), kp, vp)
+    q, bt = synth.host_bits(case.q), synth.host_bits(case.block_tables)
+    cl = synth.host_bits(case.context_lens)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.paged_decode(q, kp, vp, bt, cl, case.scale)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el > 5.0 or reps >= 200:
+            break
+    dt = el / reps
+    return {"value": decode_bytes / dt / 1e9, "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"whole batch ({q.shape[0]} seqs, {tokens} tokens), {reps} passes in "
+                      f"{el:.1f} s; decode only (fp64, std::thread over (seq, kv head))",
+            "tokens_per_s_per_layer": q.shape[0] / dt}
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import synth
+    import paged_kv_cache_58_gb300 as pkv
+    from paged_kv_cache_58_gb300 import build as pkv_build
+    if rank == 0 or ws == 1:
+        pkv_build.build()
+    if ws > 1:
+        dist.barrier()
+
+    case = synth.build_case(WORKLOAD, dev)
+    S, Hq, D = case.q.shape
+    decode_bytes, append_bytes, tokens = workload_bytes(case)
+    max_ctx = case.max_context
+    pb = pkv.auto_partition(S, max_ctx)
+    wsz = pkv.decode_workspace_bytes(S, Hq, D, max_ctx)
+    workspace = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(case.q)
+    stream = torch.cuda.current_stream(dev)
+    max_parts = math.ceil(math.ceil(max_ctx / 16) / pb)
+    launches_per_step = 2 + (1 if max_parts > 1 else 0)
+
+    def step():
+        pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new,
+                      stream=stream)
+        pkv.paged_decode(case.q, case.k_pool, case.v_pool, case.block_tables,
+                         case.context_lens, case.scale, max_context=max_ctx, out=out,
+                         partition_blocks=0, workspace=workspace, stream=stream)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < args.min_warm_seconds:
+        for _ in range(50):
+            step()
+        torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new,
+                      stream=stream)
+        ev[i][0].record(stream)
+        pkv.paged_decode(case.q, case.k_pool, case.v_pool, case.block_tables,
+                         case.context_lens, case.scale, max_context=max_ctx, out=out,
+                         partition_blocks=0, workspace=workspace, stream=stream)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert pkv.read_device_status() == 0
+
+    ms_step = total_ms / K
+    step_bytes = decode_bytes + append_bytes
+    value = ws * step_bytes / (ms_step * 1e-3) / 1e9
+    tok_s = ws * S / (ms_step * 1e-3)
+
+    # end to end through the public API with host buffers: H2D of the step's inputs
+    # from pinned memory, the two calls, D2H of the output, synchronised per step.
+    e2e = None
+    if not args.no_e2e:
+        host = {n: getattr(case, n).cpu().pin_memory() for n in
+                ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+        devb = {n: torch.empty_like(getattr(case, n)) for n in host}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            for n, t in host.items():
+                devb[n].copy_(t, non_blocking=True)
+            pkv.kv_append(case.k_pool, case.v_pool, devb["slot_mapping"], devb["k_new"],
+                          devb["v_new"], stream=stream)
+            pkv.paged_decode(devb["q"], case.k_pool, case.v_pool, devb["block_tables"],
+                             devb["context_lens"], case.scale, max_context=max_ctx, out=out,
+                             workspace=workspace, stream=stream)
+            out_h.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        if ws > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(K):
+            e2e_step()
+        el = time.perf_counter() - t0
+        if ws > 1:
+            t = torch.tensor([el], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            el = float(t.item())
+        e2e = {"value": ws * step_bytes * K / el / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": el / K * 1e3, "tokens_per_s_per_layer": ws * S * K / el}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = peaks()
+    achieved = decode_bytes / (decode_ms * 1e-3) / 1e9
+    traffic = kernel_traffic(os.path.join(ROOT, "paged_kv_cache_58_gb300", "csrc",
+                                          "paged_decode.cu"),
+                             os.path.join(ROOT, "profiles", "paged_decode_llama3_8b.md"))
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "pct_of_8tbs": 100.0 * value / ws / NOMINAL_HBM_GBS,
+        "tokens_per_s_per_layer": tok_s,
+        "config": {"workload": case.wl.name, "num_seqs": S, "q_heads": Hq,
+                   "kv_heads": case.k_pool.shape[1], "head_dim": D, "block_size": 16,
+                   "pool_blocks": case.k_pool.shape[0], "mean_context": tokens / S,
+                   "max_context": max_ctx, "partition_blocks": pb,
+                   "kv_bytes_per_step": decode_bytes, "append_bytes_per_step": append_bytes,
+                   "l2": "inputs larger than L2 (K/V read per step > 129 MB L2)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "kernel": "paged_decode (split-KV + combine)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                     "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "decode_ms": decode_ms, "traffic": traffic},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, decode_bytes, tokens)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,214 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged KV-cache attention for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (pages: "Paged Attention for Efficient Memory Management",
+ * krlt.com Triptych day 152, body and "Look closer"; "PagedAttention and
+ * RadixAttention: Let's Talk About KV Cache", aitalk.it, section "PagedAttention:
+ * Memory Like an Operating System"): each sequence's keys and values are cut into
+ * fixed-size blocks of B tokens held anywhere in one global pool; a per-sequence
+ * block table maps logical block j to a physical block id; new tokens are written
+ * into the next slot of the current block; attention walks the block table and
+ * gathers the blocks, and computes exactly ordinary softmax attention over the
+ * logically contiguous sequence.
+ *
+ * Conventions for every call below
+ *  - Pool layout (the pages fix none; this library's contract):
+ *      k_pool, v_pool: [num_blocks][num_kv_heads][block_size][head_dim], row-major,
+ *      separate tensors, same dtype.  Slot s = block * block_size + offset.
+ *  - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *  - Supported: block_size 16, head_dim 64 or 128, dtype PKV_F32 or PKV_BF16
+ *    (prefill: PKV_BF16 only), num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ *    Anything else returns PKV_ERR_UNSUPPORTED before any launch.
+ *  - Pointers marked "device" are CUDA device addresses owned by the caller; the
+ *    library never frees or retains them after the call returns, and allocates no
+ *    device memory on these paths (scratch is passed in as `workspace`).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All device work is enqueued asynchronously on it; no call synchronises except
+ *    pkv_read_device_status.
+ *  - Argument errors are detected on the host and returned synchronously before any
+ *    launch.  A failed launch returns PKV_ERR_CUDA.  Conditions only the device can
+ *    see (a slot or block id outside the pool, a pipeline wait that ran out of time)
+ *    make the kernel skip the offending access and raise a bit in the library's
+ *    device status word; read it with pkv_read_device_status.
+ *  - No C++ exception crosses this ABI.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = 1,      /* bad argument (null pointer, negative size, inconsistent shape) */
+    PKV_ERR_UNSUPPORTED = 2,  /* valid but not implemented (dtype, head_dim, block size, group) */
+    PKV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    PKV_ERR_TIMEOUT = 4,      /* device status: a bounded pipeline wait expired */
+    PKV_ERR_OOB = 5,          /* device status: a slot / block id pointed outside the pool */
+    PKV_ERR_NOMEM = 6,        /* allocator: not enough free blocks, or workspace too small */
+    PKV_ERR_NOT_FOUND = 7     /* allocator: unknown sequence id, or id already present */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Description of one K pool and one V pool (same shape and dtype). */
+typedef struct pkv_pool_desc {
+    int64_t num_blocks;   /* physical blocks in each pool */
+    int32_t block_size;   /* tokens per block (B); 16 */
+    int32_t num_kv_heads; /* Hkv */
+    int32_t head_dim;     /* D: 64 or 128 */
+    int32_t dtype;        /* pkv_dtype */
+} pkv_pool_desc;
+
+/* Static string for a status code. */
+const char* pkv_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+int pkv_version(void);
+
+/* Bytes of ONE pool (K or V) described by `pool`; 0 for an invalid description.
+ * 2 * pkv_pool_bytes(...) / (num_blocks * block_size) is the per-layer KV cost of a
+ * token, the figure the aitalk.it page quotes for Llama-3.1-70B (about 0.31 MB per
+ * token over all layers in BF16). */
+uint64_t pkv_pool_bytes(const pkv_pool_desc* pool);
+
+/* ---------------------------------------------------------------- kv_append
+ * Writes new tokens' K/V rows into their pool slots ("writes append within the
+ * current block", Triptych page, body; "append on decode", aifetchly SGLang guide,
+ * "Dynamic Node Splitting and Branch Insertion").
+ *   slot_mapping  device int64 [num_tokens]; token t goes to slot slot_mapping[t];
+ *                 a negative slot skips the token (padding).
+ *   k, v          device [num_tokens][num_kv_heads][head_dim], pool dtype, contiguous.
+ *   k_pool/v_pool device pools (see layout above), written in place.
+ * The copy is bit-exact.  A slot >= num_blocks * block_size is not written and raises
+ * PKV_ERR_OOB in the device status word.  num_tokens == 0 is a no-op. */
+pkv_status pkv_kv_append(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
+                         const int64_t* slot_mapping, const void* k, const void* v,
+                         int64_t num_tokens, void* stream);
+
+/* ---------------------------------------------------------------- paged_decode
+ * One query token per sequence attends to its first context_lens[s] tokens, gathered
+ * through block_tables (Triptych page: "the kernel walks the block table and gathers
+ * the relevant physical blocks").  Long contexts are split into partitions of
+ * `partition_blocks` blocks processed by separate CTAs and merged by a log-sum-exp
+ * combine (split-KV decode, aifetchly SGLang guide, "Integrating FlashInfer").
+ *   out           device [num_seqs][num_q_heads][head_dim], pool dtype (bf16 rounded
+ *                 to nearest even).
+ *   q             device [num_seqs][num_q_heads][head_dim], pool dtype.
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                 ceil(context_len / block_size) are never read.
+ *   context_lens  device int32 [num_seqs], each in [1, max_blocks_per_seq * block_size]
+ *                 (the token being decoded is included: write it with kv_append first).
+ *   max_context   host upper bound of context_lens (sizes the grid and workspace).
+ *   scale         softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
+ *   partition_blocks  blocks per split-KV partition; 0 lets the library choose.
+ *   workspace     device scratch of at least pkv_paged_decode_workspace_bytes(...) bytes,
+ *                 16-byte aligned; may be NULL when that size is 0.  Contents need no
+ *                 initialisation and are clobbered.
+ * Entries past context_len inside the last block may hold anything (NaN included);
+ * they never reach the output. */
+size_t pkv_paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                        int max_context, int block_size, int partition_blocks);
+pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
+                            const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int max_context, int num_seqs,
+                            int num_q_heads, float scale, int partition_blocks,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Partition size (in blocks) pkv_paged_decode uses for partition_blocks == 0; it
+ * depends only on these arguments (0 for invalid ones). */
+int pkv_paged_decode_auto_partition(int num_seqs, int max_context, int block_size);
+
+/* ---------------------------------------------------------------- paged_prefill
+ * Causal prefill of new tokens over a cached prefix ("computes only the unseen
+ * suffix" while reusing the cached prefix's K/V: aitalk.it, "RadixAttention: A Tree
+ * That Does Not Forget"; aifetchly guide, "Prefill Bypass").  Request r has
+ * cached_lens[r] tokens already in the pool followed by new_lens[r] new tokens whose
+ * K/V must already be in the pool (kv_append first).  Query row q_offsets[r] + i
+ * (i < new_lens[r]) attends keys 0 .. cached_lens[r] + i.  Runs on the tcgen05 tensor
+ * cores with TMEM accumulators; bf16 in, fp32 accumulate, bf16 out.
+ *   out, q        device [total_new][num_q_heads][head_dim] bf16.
+ *   block_tables  device int32 [num_reqs][max_blocks_per_seq].
+ *   cached_lens, new_lens  device int32 [num_reqs]; cached >= 0, new >= 0,
+ *                 cached + new <= max_blocks_per_seq * block_size.
+ *   q_offsets     device int32 [num_reqs + 1], exclusive prefix sum of new_lens.
+ *   max_new       host upper bound of new_lens (sizes the grid).
+ * Requires PKV_BF16, head_dim 128, num_q_heads / num_kv_heads == 4. */
+pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q,
+                             const void* k_pool, const void* v_pool,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* cached_lens, const int32_t* new_lens,
+                             const int32_t* q_offsets, int num_reqs, int total_new, int max_new,
+                             int num_q_heads, float scale, void* stream);
+
+/* ---------------------------------------------------------------- copy_blocks
+ * Copy-on-write support (Triptych page: "Mutation after a fork uses copy-on-write so
+ * other references stay valid"): pool[dst] = pool[src] for both pools, every kv head
+ * and slot of the block.
+ *   pairs  device int32 [num_pairs][2] = (src, dst); dst blocks must be distinct and
+ *          no dst may be another pair's src.
+ * An id outside [0, num_blocks) skips that pair and raises PKV_ERR_OOB in the device
+ * status word. */
+pkv_status pkv_copy_blocks(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
+                           const int32_t* pairs, int num_pairs, void* stream);
+
+/* ---------------------------------------------------------------- device status
+ * Synchronises `stream`, returns in *status_out the first error any kernel of this
+ * library raised on the current device since the last read (PKV_OK if none), and
+ * clears it. */
+pkv_status pkv_read_device_status(int* status_out, void* stream);
+
+/* ---------------------------------------------------------------- host block allocator
+ * Host-side (pure CPU) block manager that produces slots, block tables and
+ * copy-on-write pairs (Triptych page, body: on-demand blocks, refcounts on fork,
+ * copy-on-write on divergence, blocks return to the pool at refcount zero; khotyn.com
+ * page, "PagedAttention": a new block only when the last one is full, so at most one
+ * partially filled block per sequence).  Not thread-safe: one handle per thread.
+ * Sequence ids are caller-chosen int64 values. */
+typedef struct pkv_alloc pkv_alloc;
+
+/* New allocator over blocks [0, num_blocks).  seed == 0 hands out free blocks in
+ * ascending order; any other seed starts from a seeded shuffle of the free list (the
+ * scattered placement of a long-running server).  NULL on bad arguments. */
+pkv_alloc* pkv_alloc_create(int64_t num_blocks, int block_size, uint64_t seed);
+void pkv_alloc_destroy(pkv_alloc* a);
+
+/* Registers seq_id holding num_tokens (>= 0) tokens: ceil(num_tokens / B) new blocks.
+ * PKV_ERR_NOMEM leaves the allocator unchanged; PKV_ERR_NOT_FOUND if seq_id exists. */
+pkv_status pkv_alloc_add_seq(pkv_alloc* a, int64_t seq_id, int64_t num_tokens);
+
+/* child shares every block of parent (refcount + 1 each) and its token count. */
+pkv_status pkv_alloc_fork(pkv_alloc* a, int64_t parent, int64_t child);
+
+/* Reserves slots for n (>= 0) new tokens of seq_id, written to slots_out[n].  A new
+ * block is taken only when the last block is full.  If the last, partially filled
+ * block is shared (refcount > 1) it is first replaced by a private copy: the pair
+ * (old, new) is written to cow_pairs_out[0..1] and *num_cow_out = 1 (else 0); the
+ * caller must run pkv_copy_blocks on it before writing the slots.  On PKV_ERR_NOMEM
+ * nothing changes. */
+pkv_status pkv_alloc_append(pkv_alloc* a, int64_t seq_id, int64_t n, int64_t* slots_out,
+                            int32_t* cow_pairs_out, int* num_cow_out);
+
+/* Drops seq_id: refcount - 1 on each of its blocks; a block reaching 0 is free again. */
+pkv_status pkv_alloc_free_seq(pkv_alloc* a, int64_t seq_id);
+
+/* Host int32 [S][max_blocks] table of the given sequences, -1 padded.  PKV_ERR_INVALID
+ * if a sequence holds more than max_blocks blocks. */
+pkv_status pkv_alloc_block_table(const pkv_alloc* a, const int64_t* seq_ids, int num_seqs,
+                                 int32_t* out, int max_blocks);
+
+int64_t pkv_alloc_num_free(const pkv_alloc* a);
+int pkv_alloc_refcount(const pkv_alloc* a, int64_t block);            /* -1 if out of range */
+int64_t pkv_alloc_seq_len(const pkv_alloc* a, int64_t seq_id);        /* -1 if unknown */
+int64_t pkv_alloc_seq_num_blocks(const pkv_alloc* a, int64_t seq_id); /* -1 if unknown */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

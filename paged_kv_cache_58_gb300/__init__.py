@@ -1,0 +1,299 @@
+"""Python binding of libpkv (paged KV-cache attention on GB300 / sm_103a).
+
+Argument marshalling only: every step of the path runs in libpkv's CUDA kernels
+(see ``include/pkv.h`` for the contracts).  PyTorch provides device memory and
+the current stream.  There is no fallback: if ``libpkv.so`` is missing or a
+call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_F32 = 0
+PKV_BF16 = 1
+BLOCK_SIZE = 16
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
+           4: "device pipeline wait timed out", 5: "slot or block id outside the pool",
+           6: "out of blocks or workspace too small", 7: "unknown or duplicate sequence id"}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {_STATUS.get(status, 'unknown status')} ({status})")
+        self.status = status
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libpkv.so is not built ({LIB_PATH}); run "
+                          "paged_kv_cache_58_gb300.build.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, \
+        ctypes.c_size_t
+    P = ctypes.POINTER
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    lib.pkv_version.restype = ctypes.c_int
+    lib.pkv_pool_bytes.restype = ctypes.c_uint64
+    lib.pkv_pool_bytes.argtypes = [P(PoolDesc)]
+    lib.pkv_kv_append.restype = ctypes.c_int
+    lib.pkv_kv_append.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, i64, vp]
+    lib.pkv_paged_decode_workspace_bytes.restype = sz
+    lib.pkv_paged_decode_workspace_bytes.argtypes = [ctypes.c_int] * 6
+    lib.pkv_paged_decode_auto_partition.restype = ctypes.c_int
+    lib.pkv_paged_decode_auto_partition.argtypes = [ctypes.c_int] * 3
+    lib.pkv_paged_decode.restype = ctypes.c_int
+    lib.pkv_paged_decode.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, ctypes.c_int, vp,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, f32, ctypes.c_int,
+                                     vp, sz, vp]
+    lib.pkv_paged_prefill.restype = ctypes.c_int
+    lib.pkv_paged_prefill.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32,
+                                      vp]
+    lib.pkv_copy_blocks.restype = ctypes.c_int
+    lib.pkv_copy_blocks.argtypes = [P(PoolDesc), vp, vp, vp, ctypes.c_int, vp]
+    lib.pkv_read_device_status.restype = ctypes.c_int
+    lib.pkv_read_device_status.argtypes = [P(ctypes.c_int), vp]
+    lib.pkv_alloc_create.restype = vp
+    lib.pkv_alloc_create.argtypes = [i64, ctypes.c_int, ctypes.c_uint64]
+    lib.pkv_alloc_destroy.restype = None
+    lib.pkv_alloc_destroy.argtypes = [vp]
+    lib.pkv_alloc_add_seq.restype = ctypes.c_int
+    lib.pkv_alloc_add_seq.argtypes = [vp, i64, i64]
+    lib.pkv_alloc_fork.restype = ctypes.c_int
+    lib.pkv_alloc_fork.argtypes = [vp, i64, i64]
+    lib.pkv_alloc_append.restype = ctypes.c_int
+    lib.pkv_alloc_append.argtypes = [vp, i64, i64, P(i64), P(i32), P(ctypes.c_int)]
+    lib.pkv_alloc_free_seq.restype = ctypes.c_int
+    lib.pkv_alloc_free_seq.argtypes = [vp, i64]
+    lib.pkv_alloc_block_table.restype = ctypes.c_int
+    lib.pkv_alloc_block_table.argtypes = [vp, P(i64), ctypes.c_int, P(i32), ctypes.c_int]
+    lib.pkv_alloc_num_free.restype = i64
+    lib.pkv_alloc_num_free.argtypes = [vp]
+    lib.pkv_alloc_refcount.restype = ctypes.c_int
+    lib.pkv_alloc_refcount.argtypes = [vp, i64]
+    lib.pkv_alloc_seq_len.restype = i64
+    lib.pkv_alloc_seq_len.argtypes = [vp, i64]
+    lib.pkv_alloc_seq_num_blocks.restype = i64
+    lib.pkv_alloc_seq_num_blocks.argtypes = [vp, i64]
+    _lib = lib
+    return lib
+
+
+def lib():
+    """The loaded libpkv handle (ctypes.CDLL)."""
+    return _load()
+
+
+def _check(fn: str, st: int) -> None:
+    if st != 0:
+        raise PkvError(fn, st)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return PKV_BF16
+    if t.dtype == torch.float32:
+        return PKV_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def pool_desc(k_pool: torch.Tensor) -> PoolDesc:
+    nb, hkv, bs, d = k_pool.shape
+    return PoolDesc(nb, bs, hkv, d, _dtype_code(k_pool))
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def pool_bytes(num_blocks: int, num_kv_heads: int, head_dim: int, dtype=torch.bfloat16,
+               block_size: int = BLOCK_SIZE) -> int:
+    """Bytes of one (K or V) pool of this shape, as computed by libpkv."""
+    d = PoolDesc(num_blocks, block_size, num_kv_heads, head_dim, _dtype_code(torch.empty(0,
+                                                                                       dtype=dtype)))
+    return int(_load().pkv_pool_bytes(ctypes.byref(d)))
+
+
+def kv_append(k_pool, v_pool, slot_mapping, k, v, stream=None) -> None:
+    """Scatter k/v [T, Hkv, D] into their pool slots (slot < 0 = skip)."""
+    d = pool_desc(k_pool)
+    T = k.shape[0]
+    st = _load().pkv_kv_append(ctypes.byref(d), _dev(k_pool, "k_pool"),
+                               _dev(v_pool, "v_pool", k_pool.dtype),
+                               _dev(slot_mapping, "slot_mapping", torch.int64),
+                               _dev(k, "k", k_pool.dtype), _dev(v, "v", k_pool.dtype), T,
+                               _stream(stream))
+    _check("pkv_kv_append", st)
+
+
+def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context, partition_blocks=0):
+    return int(_load().pkv_paged_decode_workspace_bytes(num_seqs, num_q_heads, head_dim,
+                                                        max_context, BLOCK_SIZE,
+                                                        partition_blocks))
+
+
+def auto_partition(num_seqs, max_context) -> int:
+    return int(_load().pkv_paged_decode_auto_partition(num_seqs, max_context, BLOCK_SIZE))
+
+
+def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *, max_context,
+                 out=None, partition_blocks=0, workspace=None, stream=None):
+    """Decode attention: q [S, Hq, D] over the paged pools; returns out [S, Hq, D].
+
+    `max_context` is the host-side upper bound of context_lens (no device sync).
+    `workspace` (uint8 CUDA tensor) is allocated here when not given.
+    """
+    d = pool_desc(k_pool)
+    S, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    need = decode_workspace_bytes(S, Hq, D, max_context, partition_blocks)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wptr = workspace.data_ptr() if workspace is not None else None
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _load().pkv_paged_decode(ctypes.byref(d), _dev(out, "out", q.dtype),
+                                  _dev(q, "q", k_pool.dtype), _dev(k_pool, "k_pool"),
+                                  _dev(v_pool, "v_pool", k_pool.dtype),
+                                  _dev(block_tables, "block_tables", torch.int32),
+                                  block_tables.shape[1],
+                                  _dev(context_lens, "context_lens", torch.int32),
+                                  int(max_context), S, Hq, float(scale), int(partition_blocks),
+                                  wptr, wbytes, _stream(stream))
+    _check("pkv_paged_decode", st)
+    return out
+
+
+def paged_prefill(q, k_pool, v_pool, block_tables, cached_lens, new_lens, q_offsets, scale, *,
+                  max_new, out=None, stream=None):
+    """Causal prefill of q [N, Hq, D] over cached prefix + new tokens; returns out."""
+    d = pool_desc(k_pool)
+    N, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    R = cached_lens.shape[0]
+    st = _load().pkv_paged_prefill(ctypes.byref(d), _dev(out, "out", q.dtype),
+                                   _dev(q, "q", k_pool.dtype), _dev(k_pool, "k_pool"),
+                                   _dev(v_pool, "v_pool", k_pool.dtype),
+                                   _dev(block_tables, "block_tables", torch.int32),
+                                   block_tables.shape[1],
+                                   _dev(cached_lens, "cached_lens", torch.int32),
+                                   _dev(new_lens, "new_lens", torch.int32),
+                                   _dev(q_offsets, "q_offsets", torch.int32), R, N, int(max_new),
+                                   Hq, float(scale), _stream(stream))
+    _check("pkv_paged_prefill", st)
+    return out
+
+
+def copy_blocks(k_pool, v_pool, pairs, stream=None) -> None:
+    """pool[dst] = pool[src] for each row (src, dst) of int32 pairs [P, 2]."""
+    d = pool_desc(k_pool)
+    st = _load().pkv_copy_blocks(ctypes.byref(d), _dev(k_pool, "k_pool"),
+                                 _dev(v_pool, "v_pool", k_pool.dtype),
+                                 _dev(pairs, "pairs", torch.int32), pairs.shape[0],
+                                 _stream(stream))
+    _check("pkv_copy_blocks", st)
+
+
+def read_device_status(stream=None) -> int:
+    """Synchronise and return (and clear) the library's device status word."""
+    v = ctypes.c_int(0)
+    _check("pkv_read_device_status", _load().pkv_read_device_status(ctypes.byref(v),
+                                                                    _stream(stream)))
+    return v.value
+
+
+class BlockAllocator:
+    """Host block allocator (libpkv's C++ pkv_alloc): slots, tables, refcounts, CoW."""
+
+    def __init__(self, num_blocks: int, block_size: int = BLOCK_SIZE, seed: int = 0):
+        self._lib = _load()
+        self._h = self._lib.pkv_alloc_create(num_blocks, block_size, seed)
+        if not self._h:
+            raise ValueError("pkv_alloc_create: invalid arguments")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_seq(self, seq_id: int, num_tokens: int) -> None:
+        _check("pkv_alloc_add_seq", self._lib.pkv_alloc_add_seq(self._h, seq_id, num_tokens))
+
+    def fork(self, parent: int, child: int) -> None:
+        _check("pkv_alloc_fork", self._lib.pkv_alloc_fork(self._h, parent, child))
+
+    def append(self, seq_id: int, n: int = 1):
+        """Reserve n slots; returns (slots list, cow pair (old, new) or None)."""
+        slots = (ctypes.c_int64 * max(n, 1))()
+        pairs = (ctypes.c_int32 * 2)()
+        ncow = ctypes.c_int(0)
+        _check("pkv_alloc_append", self._lib.pkv_alloc_append(self._h, seq_id, n, slots, pairs,
+                                                              ctypes.byref(ncow)))
+        return list(slots[:n]), ((pairs[0], pairs[1]) if ncow.value else None)
+
+    def free_seq(self, seq_id: int) -> None:
+        _check("pkv_alloc_free_seq", self._lib.pkv_alloc_free_seq(self._h, seq_id))
+
+    def block_table(self, seq_ids, max_blocks: int) -> torch.Tensor:
+        ids = (ctypes.c_int64 * len(seq_ids))(*seq_ids)
+        out = torch.empty((len(seq_ids), max_blocks), dtype=torch.int32)
+        _check("pkv_alloc_block_table", self._lib.pkv_alloc_block_table(
+            self._h, ids, len(seq_ids),
+            ctypes.cast(out.data_ptr(), ctypes.POINTER(ctypes.c_int32)), max_blocks))
+        return out
+
+    @property
+    def num_free(self) -> int:
+        return int(self._lib.pkv_alloc_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.pkv_alloc_refcount(self._h, block))
+
+    def seq_len(self, seq_id: int) -> int:
+        return int(self._lib.pkv_alloc_seq_len(self._h, seq_id))
+
+    def seq_num_blocks(self, seq_id: int) -> int:
+        return int(self._lib.pkv_alloc_seq_num_blocks(self._h, seq_id))

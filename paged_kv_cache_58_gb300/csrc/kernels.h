@@ -1,0 +1,68 @@
+// Host-side launch interface between the C-ABI layer (pkv_api.cu) and the
+// kernel translation units.  Internal to libpkv.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Upper bound on split-KV partitions of one sequence (combine kernel's smem).
+constexpr int kMaxParts = 1024;
+
+struct DecodeArgs {
+    void* out;
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* o_part;   // [S][Hq][max_parts][D]
+    float* m_part;   // [S][Hq][max_parts]  (log2 domain)
+    float* l_part;   // [S][Hq][max_parts]
+    int* status;
+    int64_t num_blocks;
+    int max_blocks_per_seq;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int partition_blocks;
+    int max_parts;
+    float scale_log2;  // softmax scale * log2(e)
+};
+
+cudaError_t launch_paged_decode(const DecodeArgs& a, int dtype, int head_dim, int group,
+                                cudaStream_t stream);
+
+cudaError_t launch_kv_append(void* k_pool, void* v_pool, const int64_t* slot_mapping,
+                             const void* k, const void* v, int64_t num_tokens, int num_kv_heads,
+                             int row_bytes, int block_size, int64_t num_blocks, int* status,
+                             cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs,
+                               int64_t block_bytes, int64_t num_blocks, int* status,
+                               cudaStream_t stream);
+
+struct PrefillArgs {
+    void* out;
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* block_tables;
+    const int32_t* cached_lens;
+    const int32_t* new_lens;
+    const int32_t* q_offsets;
+    int* status;
+    int64_t num_blocks;
+    int max_blocks_per_seq;
+    int num_reqs;
+    int total_new;
+    int max_new;
+    int num_q_heads;
+    int num_kv_heads;
+    float scale_log2;
+};
+
+cudaError_t launch_paged_prefill(const PrefillArgs& a, int group, cudaStream_t stream);
+
+}  // namespace pkv

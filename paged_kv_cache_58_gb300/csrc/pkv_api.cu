@@ -1,0 +1,280 @@
+// C-ABI entry points of libpkv: argument validation, workspace carving and
+// kernel launches.  Declarations and contracts are in include/pkv.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/pkv.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kBlockSize = 16;
+constexpr int kMaxDevices = 64;
+constexpr double kLog2e = 1.4426950408889634;
+
+// Library device status word: first error code raised by a kernel (0 = none).
+__device__ int g_pkv_status = 0;
+
+std::mutex g_status_mu;
+int* g_status_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_pkv_status on the current device, looked up once per device
+// (a __device__ symbol's host-side name is not a device address).
+int* status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pkv_status) != cudaSuccess) return nullptr;
+        g_status_addr[dev] = static_cast<int*>(p);
+    }
+    return g_status_addr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(int dtype) { return dtype == PKV_BF16 ? 2 : 4; }
+
+pkv_status check_pool(const pkv_pool_desc* pool) {
+    if (!pool) return PKV_ERR_INVALID;
+    if (pool->num_blocks <= 0 || pool->num_kv_heads <= 0 || pool->head_dim <= 0 ||
+        pool->block_size <= 0)
+        return PKV_ERR_INVALID;
+    if (pool->dtype != PKV_F32 && pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (pool->block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+    if (pool->head_dim != 64 && pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (pool->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if (pool->num_blocks > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+pkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// Partition policy for split-KV decode: at least 32 blocks (512 tokens) per
+// partition so the partial write + combine read stay ~2% of the K/V bytes, at
+// most 64 partitions per sequence to bound the workspace; shrink partitions
+// (down to 8 blocks) while fewer than 2 x 152 CTAs would be busy.
+// The CTA estimate counts one kv head per sequence so that the choice, and with it
+// the workspace size, depends on (num_seqs, max_context) only.
+int auto_partition(int num_seqs, int max_context) {
+    const int max_blocks = ceil_div(max_context, kBlockSize);
+    int pb = ceil_div(max_blocks, 64);
+    if (pb < 32) pb = 32;
+    pb = (pb + 3) / 4 * 4;
+    while (pb > 8 && static_cast<int64_t>(num_seqs) * ceil_div(max_blocks, pb) < 304) pb /= 2;
+    return pb;
+}
+
+size_t decode_workspace(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
+    if (max_parts <= 1) return 0;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
+    const size_t o = rows * head_dim * sizeof(float);
+    const size_t ml = (rows * sizeof(float) + 15) / 16 * 16;
+    return o + 2 * ml;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PKV_ERR_CUDA: return "CUDA error";
+        case PKV_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case PKV_ERR_OOB: return "slot or block id outside the pool";
+        case PKV_ERR_NOMEM: return "out of blocks or workspace too small";
+        case PKV_ERR_NOT_FOUND: return "unknown or duplicate sequence id";
+        default: return "unknown status";
+    }
+}
+
+int pkv_version(void) { return 100; }
+
+uint64_t pkv_pool_bytes(const pkv_pool_desc* pool) {
+    if (!pool || pool->num_blocks <= 0 || pool->block_size <= 0 || pool->num_kv_heads <= 0 ||
+        pool->head_dim <= 0 || (pool->dtype != PKV_F32 && pool->dtype != PKV_BF16))
+        return 0;
+    return static_cast<uint64_t>(pool->num_blocks) * pool->num_kv_heads * pool->block_size *
+           pool->head_dim * elem_bytes(pool->dtype);
+}
+
+pkv_status pkv_kv_append(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
+                         const int64_t* slot_mapping, const void* k, const void* v,
+                         int64_t num_tokens, void* stream) {
+    pkv_status st = check_pool(pool);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return PKV_ERR_INVALID;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_pool || !v_pool || !slot_mapping || !k || !v) return PKV_ERR_INVALID;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k) || !aligned16(v))
+        return PKV_ERR_INVALID;
+    int* status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    const int row_bytes = pool->head_dim * elem_bytes(pool->dtype);
+    return from_cuda(pkv::launch_kv_append(k_pool, v_pool, slot_mapping, k, v, num_tokens,
+                                           pool->num_kv_heads, row_bytes, pool->block_size,
+                                           pool->num_blocks, status,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+int pkv_paged_decode_auto_partition(int num_seqs, int max_context, int block_size) {
+    if (num_seqs <= 0 || max_context <= 0 || block_size != kBlockSize) return 0;
+    return auto_partition(num_seqs, max_context);
+}
+
+size_t pkv_paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                        int max_context, int block_size, int partition_blocks) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context <= 0 ||
+        block_size != kBlockSize || partition_blocks < 0)
+        return 0;
+    const int pb = partition_blocks ? partition_blocks : auto_partition(num_seqs, max_context);
+    const int max_parts = ceil_div(ceil_div(max_context, kBlockSize), pb);
+    return decode_workspace(num_seqs, num_q_heads, head_dim, max_parts);
+}
+
+pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
+                            const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int max_context, int num_seqs,
+                            int num_q_heads, float scale, int partition_blocks,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    pkv_status st = check_pool(pool);
+    if (st != PKV_OK) return st;
+    if (num_seqs < 0 || num_q_heads <= 0 || partition_blocks < 0) return PKV_ERR_INVALID;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens)
+        return PKV_ERR_INVALID;
+    if (max_blocks_per_seq <= 0 || max_context <= 0 ||
+        static_cast<int64_t>(max_context) > static_cast<int64_t>(max_blocks_per_seq) * kBlockSize)
+        return PKV_ERR_INVALID;
+    if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID;
+    const int group = num_q_heads / pool->num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PKV_ERR_INVALID;
+
+    const int pb = partition_blocks ? partition_blocks : auto_partition(num_seqs, max_context);
+    const int max_parts = ceil_div(ceil_div(max_context, kBlockSize), pb);
+    if (max_parts > pkv::kMaxParts) return PKV_ERR_UNSUPPORTED;
+    const size_t need = decode_workspace(num_seqs, num_q_heads, pool->head_dim, max_parts);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+        return PKV_ERR_NOMEM;
+    int* status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+
+    pkv::DecodeArgs a{};
+    a.out = out;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.status = status;
+    a.num_blocks = pool->num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = pool->num_kv_heads;
+    a.partition_blocks = pb;
+    a.max_parts = max_parts;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    if (need > 0) {
+        const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
+        const size_t ml = (rows * sizeof(float) + 15) / 16 * 16;
+        char* w = static_cast<char*>(workspace);
+        a.o_part = reinterpret_cast<float*>(w);
+        a.m_part = reinterpret_cast<float*>(w + rows * pool->head_dim * sizeof(float));
+        a.l_part = reinterpret_cast<float*>(w + rows * pool->head_dim * sizeof(float) + ml);
+    }
+    return from_cuda(pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q,
+                             const void* k_pool, const void* v_pool,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* cached_lens, const int32_t* new_lens,
+                             const int32_t* q_offsets, int num_reqs, int total_new, int max_new,
+                             int num_q_heads, float scale, void* stream) {
+    pkv_status st = check_pool(pool);
+    if (st != PKV_OK) return st;
+    if (num_reqs < 0 || total_new < 0 || max_new < 0 || num_q_heads <= 0)
+        return PKV_ERR_INVALID;
+    if (num_reqs == 0 || total_new == 0 || max_new == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !cached_lens || !new_lens ||
+        !q_offsets || max_blocks_per_seq <= 0)
+        return PKV_ERR_INVALID;
+    if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID;
+    const int group = num_q_heads / pool->num_kv_heads;
+    if (pool->dtype != PKV_BF16 || pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_ERR_UNSUPPORTED;
+    if (num_reqs > 65535) return PKV_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PKV_ERR_INVALID;
+    int* status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    pkv::PrefillArgs a{};
+    a.out = out;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.block_tables = block_tables;
+    a.cached_lens = cached_lens;
+    a.new_lens = new_lens;
+    a.q_offsets = q_offsets;
+    a.status = status;
+    a.num_blocks = pool->num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_reqs = num_reqs;
+    a.total_new = total_new;
+    a.max_new = max_new;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = pool->num_kv_heads;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    const cudaError_t e = pkv::launch_paged_prefill(a, group, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
+pkv_status pkv_copy_blocks(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
+                           const int32_t* pairs, int num_pairs, void* stream) {
+    pkv_status st = check_pool(pool);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0) return PKV_ERR_INVALID;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_pool || !v_pool || !pairs) return PKV_ERR_INVALID;
+    if (!aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID;
+    if (num_pairs > 65535 * 1024) return PKV_ERR_UNSUPPORTED;
+    int* status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    const int64_t block_bytes = static_cast<int64_t>(pool->num_kv_heads) * pool->block_size *
+                                pool->head_dim * elem_bytes(pool->dtype);
+    return from_cuda(pkv::launch_copy_blocks(k_pool, v_pool, pairs, num_pairs, block_bytes,
+                                             pool->num_blocks, status,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_read_device_status(int* status_out, void* stream) {
+    if (!status_out) return PKV_ERR_INVALID;
+    int* status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    *status_out = v;
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,199 @@
+"""CPU-only checks of libpkv: exported symbols, host allocator invariants, page figures.
+
+No kernel is launched here; the library is loaded and only its host functions run.
+"""
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden", "pages_figures.json")
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_58_gb300 import build
+    build.build()
+    import paged_kv_cache_58_gb300 as m
+    return m
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(pkv_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_function(pkv):
+    names = declared_functions()
+    assert len(names) >= 20
+    lib = pkv.lib()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(pkv):
+    lib = pkv.lib()
+    assert lib.pkv_status_string(0) == b"ok"
+    assert lib.pkv_status_string(5).startswith(b"slot")
+    assert lib.pkv_version() >= 100
+
+
+def test_pool_bytes_and_llama70b_figure(pkv):
+    g = json.load(open(GOLDEN))["kv_bytes_per_token_llama31_70b"]
+    sh = g["shape_used"]
+    import torch
+    one_block = pkv.pool_bytes(1, sh["kv_heads"], sh["head_dim"], torch.bfloat16)
+    assert one_block == 16 * sh["kv_heads"] * sh["head_dim"] * 2
+    per_token = 2 * sh["layers"] * one_block / 16           # K and V, all layers
+    assert per_token == 327680
+    assert round(per_token / 2**20, 2) == g["mb_per_token"]
+    assert abs(per_token * g["context_tokens"] / 2**30 - g["context_gb"]) < 1.0
+
+
+def test_sixty_token_response_takes_four_blocks(pkv):
+    g = json.load(open(GOLDEN))["sixty_token_response"]
+    a = pkv.BlockAllocator(100)
+    a.add_seq(1, 0)
+    for _ in range(g["tokens"]):
+        a.append(1, 1)
+    assert a.seq_num_blocks(1) == g["blocks"]
+    assert a.seq_num_blocks(1) * g["block_size"] - g["tokens"] <= g["max_idle_slots"]
+    assert a.num_free == 100 - g["blocks"]
+
+
+def _invariants(a, seqs):
+    held = {}
+    used = set()
+    for sid in seqs:
+        n = a.seq_num_blocks(sid)
+        L = a.seq_len(sid)
+        assert 0 <= n * 16 - L < 16 or (L == 0 and n == 0), (sid, n, L)
+        row = a.block_table([sid], max(n, 1))[0].tolist()
+        for b in row[:n]:
+            held[b] = held.get(b, 0) + 1
+            used.add(b)
+    for b, cnt in held.items():
+        assert a.refcount(b) == cnt
+    assert a.num_free + len(used) == a.num_blocks
+
+
+def test_random_workload_waste_bound_and_conservation(pkv):
+    g = json.load(open(GOLDEN))["waste_bound"]
+    assert g["max_partial_blocks_per_sequence"] == 1
+    rng = np.random.default_rng(0)
+    a = pkv.BlockAllocator(4000, seed=3)
+    live = []
+    nxt = 0
+    for step in range(600):
+        op = rng.random()
+        if op < 0.3 or not live:
+            a.add_seq(nxt, int(rng.integers(0, 200)))
+            live.append(nxt)
+            nxt += 1
+        elif op < 0.45:
+            parent = live[int(rng.integers(len(live)))]
+            a.fork(parent, nxt)
+            live.append(nxt)
+            nxt += 1
+        elif op < 0.85:
+            sid = live[int(rng.integers(len(live)))]
+            a.append(sid, int(rng.integers(1, 40)))
+        else:
+            sid = live.pop(int(rng.integers(len(live))))
+            a.free_seq(sid)
+        if step % 50 == 0:
+            _invariants(a, live)
+    _invariants(a, live)
+    for sid in live:
+        a.free_seq(sid)
+    assert a.num_free == 4000
+    assert all(a.refcount(b) == 0 for b in range(4000))
+
+
+def test_fork_shares_then_cow_on_partial_block(pkv):
+    a = pkv.BlockAllocator(10)
+    a.add_seq(0, 20)                        # blocks 0, 1 (block 1 holds 4 tokens)
+    assert a.block_table([0], 3)[0].tolist() == [0, 1, -1]
+    a.fork(0, 1)
+    assert a.refcount(0) == 2 and a.refcount(1) == 2 and a.num_free == 8
+    slots, cow = a.append(1, 1)
+    assert cow == (1, 2)                   # private copy of the shared partial block
+    assert slots == [2 * 16 + 4]
+    assert a.refcount(1) == 1 and a.refcount(2) == 1 and a.refcount(0) == 2
+    slots, cow = a.append(0, 1)            # parent's block 1 is private again
+    assert cow is None and slots == [1 * 16 + 4]
+    a.free_seq(0)
+    assert a.refcount(0) == 1 and a.refcount(1) == 0
+    a.free_seq(1)
+    assert a.num_free == 10
+
+
+def test_fork_at_block_boundary_needs_no_copy(pkv):
+    a = pkv.BlockAllocator(10)
+    a.add_seq(0, 32)
+    a.fork(0, 1)
+    slots, cow = a.append(1, 3)
+    assert cow is None
+    assert slots == [2 * 16, 2 * 16 + 1, 2 * 16 + 2]
+
+
+def test_out_of_blocks_leaves_state_unchanged(pkv):
+    import paged_kv_cache_58_gb300 as m
+    a = pkv.BlockAllocator(4)
+    a.add_seq(0, 50)                        # 4 blocks
+    with pytest.raises(m.PkvError) as e:
+        a.add_seq(1, 1)
+    assert e.value.status == 6
+    with pytest.raises(m.PkvError):
+        a.append(0, 15)
+    assert a.seq_len(0) == 50 and a.num_free == 0
+    slots, _ = a.append(0, 14)              # fills the last block exactly
+    assert len(slots) == 14 and a.seq_len(0) == 64
+
+
+def test_seeded_free_order(pkv):
+    a0 = pkv.BlockAllocator(64)
+    a0.add_seq(0, 64 * 16)
+    assert a0.block_table([0], 64)[0].tolist() == list(range(64))
+    a1 = pkv.BlockAllocator(64, seed=7)
+    a1.add_seq(0, 64 * 16)
+    t1 = a1.block_table([0], 64)[0].tolist()
+    assert sorted(t1) == list(range(64)) and t1 != list(range(64))
+    a2 = pkv.BlockAllocator(64, seed=7)
+    a2.add_seq(0, 64 * 16)
+    assert a2.block_table([0], 64)[0].tolist() == t1
+
+
+def test_unknown_ids_and_small_tables(pkv):
+    import paged_kv_cache_58_gb300 as m
+    a = pkv.BlockAllocator(8)
+    a.add_seq(0, 40)
+    with pytest.raises(m.PkvError):
+        a.add_seq(0, 1)
+    with pytest.raises(m.PkvError):
+        a.fork(5, 6)
+    with pytest.raises(m.PkvError):
+        a.block_table([0], 2)
+    with pytest.raises(m.PkvError):
+        a.free_seq(9)
+
+
+def test_decode_workspace_and_partition_policy(pkv):
+    # 8B-shaped batch: 64 sequences up to 4096 tokens -> 512-token partitions
+    assert pkv.auto_partition(64, 4096) == 32
+    ws = pkv.decode_workspace_bytes(64, 32, 128, 4096)
+    assert ws == 64 * 32 * 8 * (128 + 2) * 4
+    # 70B-shaped batch: 131072 tokens -> at most 64 partitions
+    pb = pkv.auto_partition(16, 131072)
+    assert pb == 128 and -(-8192 // pb) == 64
+    # a single short sequence needs no workspace
+    assert pkv.decode_workspace_bytes(1, 8, 128, 64) == 0
