@@ -207,7 +207,7 @@ pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q
                              int num_q_heads, float scale, void* stream) {
     pkv_status st = check_pool(pool);
     if (st != PKV_OK) return st;
-    if (num_reqs < 0 || total_new < 0 || max_new < 0 || num_q_heads <= 0)
+    if (num_reqs < 0 || total_new < 0 || max_new < 0 || num_q_heads <= 0 || !(scale > 0.f))
         return PKV_ERR_INVALID;
     if (num_reqs == 0 || total_new == 0 || max_new == 0) return PKV_OK;
     if (!out || !q || !k_pool || !v_pool || !block_tables || !cached_lens || !new_lens ||

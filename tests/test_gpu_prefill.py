@@ -1,0 +1,96 @@
+"""GPU parity of the tcgen05 prefix-chunk prefill against the fp64 oracle (C ABI)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests.helpers import check_attention, oracle_prefill_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_58_gb300 as m
+    from paged_kv_cache_58_gb300 import build
+    build.build()
+    return m
+
+
+def run_prefill(pkv, case):
+    pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new)
+    out = pkv.paged_prefill(case.q, case.k_pool, case.v_pool, case.block_tables,
+                            case.cached_lens, case.new_lens, case.q_offsets, case.scale,
+                            max_new=int(case.new_lens.max()))
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    return out
+
+
+def custom_case(hq, hkv, cached, new, seed, num_blocks=1024):
+    """Prefill case with per-request new lengths (the workload recipe fixes n)."""
+    wl = dataclasses.replace(synth.WORKLOADS["prefill"], num_q_heads=hq, num_kv_heads=hkv,
+                             new_tokens=max(new), num_blocks=num_blocks)
+    case = synth.build_case(wl, "cuda", lengths=cached, seed=seed)
+    if all(x == max(new) for x in new):
+        return case
+    # keep the first new[r] tokens of each request: rebuild q / k_new / slots compactly
+    n_max = max(new)
+    keep = np.concatenate([np.arange(r * n_max, r * n_max + new[r]) for r in range(len(new))])
+    keep_t = torch.as_tensor(keep, device="cuda")
+    # drop the unused new tokens' pool slots back to NaN-free state is unnecessary: they
+    # lie past each request's end and are never read as valid keys.
+    case.q = case.q[keep_t].contiguous()
+    case.k_new = case.k_new[keep_t].contiguous()
+    case.v_new = case.v_new[keep_t].contiguous()
+    case.slot_mapping = case.slot_mapping[keep_t].contiguous()
+    case.new_lens = torch.tensor(new, dtype=torch.int32, device="cuda")
+    case.q_offsets = torch.tensor(np.concatenate([[0], np.cumsum(new)]), dtype=torch.int32,
+                                  device="cuda")
+    case.context_lens = case.cached_lens + case.new_lens
+    return case
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 8), (64, 8)])
+def test_prefill_small_mixed(pkv, oracle_mod, hq, hkv):
+    cached = [0, 100, 1000, 16, 33]
+    new = [37, 64, 300, 1, 128]
+    case = custom_case(hq, hkv, cached, new, seed=hq)
+    ref, _, _ = oracle_prefill_case(oracle_mod, case)
+    check_attention(run_prefill(pkv, case), ref)
+
+
+@pytest.mark.parametrize("cached,new", [([0], [1]), ([0], [128]), ([0], [129]), ([127], [1]),
+                                        ([128], [128]), ([4095], [257]), ([1], [511])])
+def test_prefill_edges(pkv, oracle_mod, cached, new):
+    case = custom_case(32, 8, cached, new, seed=cached[0] + new[0])
+    ref, _, _ = oracle_prefill_case(oracle_mod, case)
+    check_attention(run_prefill(pkv, case), ref)
+
+
+def test_prefill_last_row_equals_decode(pkv, oracle_mod):
+    """The last prefill row of a request equals a decode of that token (two kernels)."""
+    case = custom_case(32, 8, [700], [40], seed=5)
+    out = run_prefill(pkv, case)
+    q_last = case.q[-1:].contiguous()
+    dec = pkv.paged_decode(q_last, case.k_pool, case.v_pool, case.block_tables,
+                           case.context_lens, case.scale, max_context=740)
+    torch.cuda.synchronize()
+    ref, _, _ = oracle_prefill_case(oracle_mod, case)
+    check_attention(dec, ref[-1:])
+    check_attention(out[-1:], ref[-1:])
+
+
+def test_prefix_cached_prefill_published_config_sampled(pkv, oracle_mod):
+    """Published prefill workload at full size (16 x 512 new tokens); sampled rows."""
+    case = synth.build_case("prefill", "cuda")
+    N, Hq = case.q.shape[:2]
+    want = synth.sample_rows(N, Hq, 512, seed=5)
+    ref, _, _ = oracle_prefill_case(oracle_mod, case, want=want)
+    out = run_prefill(pkv, case)
+    check_attention(out, ref, mask=want)
+    assert torch.isfinite(out.float()).all()
