@@ -2,6 +2,7 @@
 // kernel translation units.  Internal to libpkv.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -31,8 +32,22 @@ struct DecodeArgs {
     float scale_log2;  // softmax scale * log2(e)
 };
 
+// CUDA-core decode (fp32 and bf16 pools): split kernel + combine.
 cudaError_t launch_paged_decode(const DecodeArgs& a, int dtype, int head_dim, int group,
                                 cudaStream_t stream);
+// Tensor-core decode for bf16 pools (warp-level MMA): split kernel + combine.
+cudaError_t launch_paged_decode_tc(const DecodeArgs& a, int head_dim, int group,
+                                   cudaStream_t stream);
+// Log-sum-exp merge of the split-KV partials into `out`.
+cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, int head_dim,
+                                  cudaStream_t stream);
+
+// Tensor maps (host): a pool viewed as rows [num_blocks * Hkv * 16] x head_dim bf16,
+// box 64 columns x 16 rows, 128-byte swizzle.
+bool make_pool_map(CUtensorMap* m, const void* pool, int64_t rows, int head_dim);
+// q [tokens][Hq][head_dim] bf16 read as boxes of 64 columns x G heads x tok tokens.
+bool make_q_group_map(CUtensorMap* m, const void* q, int tokens, int hq, int head_dim, int G,
+                      int tok);
 
 cudaError_t launch_kv_append(void* k_pool, void* v_pool, const int64_t* slot_mapping,
                              const void* k, const void* v, int64_t num_tokens, int num_kv_heads,

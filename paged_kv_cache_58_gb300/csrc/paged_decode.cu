@@ -404,9 +404,18 @@ decode_combine_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int w = 0; w < D / 32; ++w) W += red[w];
 
+    // Independent loads, 8 partitions at a time, so the partial reads overlap.
     const float* op = a.o_part + row * a.max_parts * D + d;
     float acc = 0.f;
-    for (int p = 0; p < np; ++p) acc = fmaf(wsm[p], op[static_cast<size_t>(p) * D], acc);
+    int p = 0;
+    for (; p + 8 <= np; p += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(op + static_cast<size_t>(p + u) * D);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc = fmaf(wsm[p + u], v[u], acc);
+    }
+    for (; p < np; ++p) acc = fmaf(wsm[p], __ldg(op + static_cast<size_t>(p) * D), acc);
     store_elem<T>(static_cast<T*>(a.out) + row * D + d, acc / W);
 }
 
@@ -426,6 +435,12 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 template <typename T, int D>
+cudaError_t launch_combine_typed(const DecodeArgs& a, cudaStream_t stream) {
+    decode_combine_kernel<T, D><<<dim3(a.num_q_heads, a.num_seqs), D, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
 cudaError_t launch_group(const DecodeArgs& a, int G, cudaStream_t stream) {
     switch (G) {
         case 1: return launch_typed<T, D, 1>(a, stream);
@@ -437,6 +452,18 @@ cudaError_t launch_group(const DecodeArgs& a, int G, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, int head_dim,
+                                  cudaStream_t stream) {
+    if (dtype == PKV_BF16) {
+        if (head_dim == 128) return launch_combine_typed<uint16_t, 128>(a, stream);
+        if (head_dim == 64) return launch_combine_typed<uint16_t, 64>(a, stream);
+    } else if (dtype == PKV_F32) {
+        if (head_dim == 128) return launch_combine_typed<float, 128>(a, stream);
+        if (head_dim == 64) return launch_combine_typed<float, 64>(a, stream);
+    }
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, int dtype, int head_dim, int group,
                                 cudaStream_t stream) {

@@ -12,8 +12,12 @@
 // every K/V tile it stages serves all G heads.  Per 128-key KV tile:
 //   S = Q K^T     tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) -> TMEM
 //   softmax       4 warps, one thread per row: tcgen05.ld S, causal mask, exp2,
-//                 row sums in fp32, P -> shared memory (bf16, 128B-swizzled)
-//   O += P V      tcgen05.mma into a TMEM accumulator that lives across tiles
+//                 row sums in fp32; P is split into bf16 hi + lo parts (P = hi + lo
+//                 to ~2^-17 relative) stored to TMEM with tcgen05.st
+//   O += P V      two tcgen05.mma passes (A = P hi, then P lo, read from TMEM; B = V
+//                 from shared memory) into a TMEM accumulator that lives across tiles
+// The split keeps the probabilities at fp32-like precision: a single bf16 P is off by
+// up to 2^-9 per weight, which rows attending only a few keys do not average away.
 // The running max is updated lazily: O and l are rescaled only when a row's max
 // grows by more than 2^8, which keeps P <= 256 and leaves the result exact.
 //
@@ -22,12 +26,10 @@
 // tiles are double-buffered; each 16-token block of a tile arrives as two TMA
 // boxes (64 columns x 16 rows, 128-byte swizzle) per pool.
 //
-// TMEM columns: S buffers at [0, 128) and [128, 256), O at [256, 384).
+// TMEM columns: S buffers at [0, 128) and [128, 256), O at [256, 384), P hi at
+// [384, 448) and P lo at [448, 512) (two bf16 per column).
 #include <cuda.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -48,8 +50,7 @@ constexpr int kStages = 2;
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffP = kOffV + kStages * kTileBytes;
-constexpr int kOffBar = kOffP + kTileBytes;
+constexpr int kOffBar = kOffV + kStages * kTileBytes;
 constexpr int kNumBars = 12;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1 KB alignment slack
 constexpr int kThreads = 192;
@@ -154,7 +155,6 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t sQ = smem_u32(smem + kOffQ);
     const uint32_t sK = smem_u32(smem + kOffK);
     const uint32_t sV = smem_u32(smem + kOffV);
-    const uint32_t sP = smem_u32(smem + kOffP);
 
     if (warp == 4) {
         // ------------------------------------------------------------ TMA producer
@@ -220,10 +220,10 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < kKeys / 16; ++ks) {
-                        const uint32_t aoff = (ks >> 2) * kHalf + (ks & 3) * 32;
-                        umma_bf16(tO, smem_desc_sw128(sP + aoff, 16, 1024),
-                                  smem_desc_sw128(sV + sj * kTileBytes + ks * 2048, kHalf, 1024),
-                                  idesc_pv, (j > 0) || (ks > 0));
+                        const uint64_t bv =
+                            smem_desc_sw128(sV + sj * kTileBytes + ks * 2048, kHalf, 1024);
+                        umma_bf16_ta(tO, tmem + 384 + ks * 8, bv, idesc_pv, (j > 0) || (ks > 0));
+                        umma_bf16_ta(tO, tmem + 448 + ks * 8, bv, idesc_pv, true);
                     }
                     umma_commit(&bars[BPV_DONE]);
                     umma_commit(&bars[BKV_EMPTY + sj]);
@@ -273,13 +273,17 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             const float m_cur = grow ? m_tile : m_used;
             const float alpha = fast_exp2(m_used - m_cur);   // 1 unless grow; 0 at start
             float rs = 0.f;
-            uint32_t pk[kKeys / 2];
+            float phi[kKeys / 2], plo[kKeys / 2];   // packed bf16 pairs, as fp32 bit patterns
 #pragma unroll
             for (int k = 0; k < kKeys; k += 2) {
                 const float p0 = fast_exp2(fmaf(x[k], sl2, -m_cur));
                 const float p1 = fast_exp2(fmaf(x[k + 1], sl2, -m_cur));
                 rs += p0 + p1;
-                pk[k / 2] = pack_bf16x2(p0, p1);
+                const uint32_t h = pack_bf16x2(p0, p1);
+                const float r0 = p0 - bf16lo_to_f32(h);
+                const float r1 = p1 - bf16hi_to_f32(h);
+                phi[k / 2] = __uint_as_float(h);
+                plo[k / 2] = __uint_as_float(pack_bf16x2(r0, r1));
             }
             l = l * alpha + rs;
             m_used = m_cur;
@@ -303,15 +307,15 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
                 tmem_wait_st();
             }
-            // P row -> shared memory, K-major with the 128-byte swizzle the MMA expects.
-            uint8_t* prow = smem + kOffP + row * 128;
+            // P row -> TMEM (this thread's lane), hi and lo parts.
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                const int half = ch >> 3;
-                const int j = ch & 7;
-                uint4 v4 = make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-                *reinterpret_cast<uint4*>(prow + half * kHalf + ((j ^ (row & 7)) << 4)) = v4;
+            for (int q = 0; q < 2; ++q) {
+                tmem_st32(tmem + lane_addr + 384 + q * 32,
+                          *reinterpret_cast<float(*)[32]>(&phi[q * 32]));
+                tmem_st32(tmem + lane_addr + 448 + q * 32,
+                          *reinterpret_cast<float(*)[32]>(&plo[q * 32]));
             }
+            tmem_wait_st();
             // Keys past the last one this tile needs are masked for every row, but their
             // V rows may hold anything (NaN in unused slots, stale data where no block was
             // loaded this tile); zero them so that 0 * V stays 0 in the P.V product.
@@ -365,56 +369,12 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
 }
 
-// ---------------------------------------------------------------- tensor maps
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// Pool viewed as rows [num_blocks * Hkv * 16] x 128 bf16; box 64 columns x 16 rows.
-bool make_pool_map(CUtensorMap* m, const void* pool, int64_t rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHead), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {kHead * 2};
-    cuuint32_t box[2] = {64, kBlk};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
-// q viewed as [tokens][Hq][128]; box 64 columns x G heads x TOK tokens.
-bool make_q_map(CUtensorMap* m, const void* q, int tokens, int hq, int G) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHead), static_cast<cuuint64_t>(hq),
-                          static_cast<cuuint64_t>(tokens)};
-    cuuint64_t strides[2] = {kHead * 2, static_cast<cuuint64_t>(hq) * kHead * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kRows / G)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
 template <int G>
 cudaError_t launch_g(const PrefillArgs& a, cudaStream_t stream) {
     CUtensorMap mq, mk, mv;
     const int64_t rows = a.num_blocks * a.num_kv_heads * kBlk;
-    if (!make_q_map(&mq, a.q, a.total_new, a.num_q_heads, G) ||
-        !make_pool_map(&mk, a.k_pool, rows) || !make_pool_map(&mv, a.v_pool, rows))
+    if (!make_q_group_map(&mq, a.q, a.total_new, a.num_q_heads, kHead, G, kRows / G) ||
+        !make_pool_map(&mk, a.k_pool, rows, kHead) || !make_pool_map(&mv, a.v_pool, rows, kHead))
         return cudaErrorInvalidValue;
     auto kern = prefill_tcgen05_kernel<G>;
     cudaError_t e =

@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/pkv.h"
@@ -68,6 +70,13 @@ int auto_partition(int num_seqs, int max_context) {
     pb = (pb + 3) / 4 * 4;
     while (pb > 8 && static_cast<int64_t>(num_seqs) * ceil_div(max_blocks, pb) < 304) pb /= 2;
     return pb;
+}
+
+// bf16 decode runs on the tensor-core kernel; PKV_DECODE_KERNEL=simt selects the
+// CUDA-core kernel instead (read at each call; used to test and compare the two).
+bool decode_use_simt() {
+    const char* v = std::getenv("PKV_DECODE_KERNEL");
+    return v != nullptr && std::strcmp(v, "simt") == 0;
 }
 
 size_t decode_workspace(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
@@ -195,8 +204,10 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
         a.m_part = reinterpret_cast<float*>(w + rows * pool->head_dim * sizeof(float));
         a.l_part = reinterpret_cast<float*>(w + rows * pool->head_dim * sizeof(float) + ml);
     }
-    return from_cuda(pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group,
-                                              static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+    if (pool->dtype == PKV_BF16 && !decode_use_simt())
+        return from_cuda(pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_));
+    return from_cuda(pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_));
 }
 
 pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q,

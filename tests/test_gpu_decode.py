@@ -21,6 +21,16 @@ def pkv():
     return m
 
 
+@pytest.fixture(params=["tc", "simt"])
+def kernel(request, monkeypatch):
+    """bf16 decode kernel under test: tensor-core (default) or CUDA-core."""
+    if request.param == "simt":
+        monkeypatch.setenv("PKV_DECODE_KERNEL", "simt")
+    else:
+        monkeypatch.delenv("PKV_DECODE_KERNEL", raising=False)
+    return request.param
+
+
 def run_decode(pkv, case, partition_blocks=0):
     pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new)
     out = pkv.paged_decode(case.q, case.k_pool, case.v_pool, case.block_tables,
@@ -56,7 +66,7 @@ EDGE_LENS = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 500, 1000]
 @pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (64, 8, 128), (16, 8, 128), (8, 8, 128),
                                       (32, 8, 64), (8, 1, 64)])
 @pytest.mark.parametrize("pb", [0, 1, 5])
-def test_edge_lengths_bf16(pkv, oracle_mod, hq, hkv, d, pb):
+def test_edge_lengths_bf16(pkv, oracle_mod, hq, hkv, d, pb, kernel):
     wl = small("8b", num_q_heads=hq, num_kv_heads=hkv, head_dim=d, num_blocks=512)
     case = synth.build_case(wl, "cuda", lengths=EDGE_LENS, seed=hq * 7 + d + pb)
     ref, kp, vp = oracle_decode_case(oracle_mod, case)
@@ -73,7 +83,7 @@ def test_fp32_shapes(pkv, oracle_mod, hq, hkv):
     check_attention(run_decode(pkv, case, partition_blocks=2), ref)
 
 
-def test_llama3_8b_decode_full(pkv, oracle_mod):
+def test_llama3_8b_decode_full(pkv, oracle_mod, kernel):
     """Published 8B-shaped batch at full size, every output vs the oracle."""
     case = synth.build_case("8b", "cuda")
     ref, kp, vp = oracle_decode_case(oracle_mod, case)
@@ -82,7 +92,7 @@ def test_llama3_8b_decode_full(pkv, oracle_mod):
     check_attention(out, ref)
 
 
-def test_llama31_70b_long_decode_sampled(pkv, oracle_mod):
+def test_llama31_70b_long_decode_sampled(pkv, oracle_mod, kernel):
     """Published 70B long-context batch at full size; sampled (seq, head) outputs."""
     case = synth.build_case("70b", "cuda")
     S, Hq = case.q.shape[:2]
@@ -106,7 +116,7 @@ def test_shared_prefix_decode_sampled(pkv, oracle_mod):
     assert torch.isfinite(out.float()).all()
 
 
-def test_shared_prefix_equals_copied_prefix_on_gpu(pkv):
+def test_shared_prefix_equals_copied_prefix_on_gpu(pkv, kernel):
     """Same bits whether the prefix blocks are shared or copied per sequence."""
     wl = small("shared", num_seqs=6, num_blocks=4096)
     case = synth.build_case(wl, "cuda", lengths=[64, 100, 1024, 65, 300, 17])
@@ -131,7 +141,7 @@ def test_shared_prefix_equals_copied_prefix_on_gpu(pkv):
     assert torch.equal(out_shared.view(torch.int16), out_copied.view(torch.int16))
 
 
-def test_permuted_placement_same_bits(pkv):
+def test_permuted_placement_same_bits(pkv, kernel):
     """Moving every block to another physical id leaves the output bits unchanged."""
     wl = small("8b", num_seqs=5, num_blocks=2048)
     case = synth.build_case(wl, "cuda", lengths=[700, 33, 4096, 1, 1500], seed=77)
