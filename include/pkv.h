@@ -124,6 +124,31 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
  * depends only on these arguments (0 for invalid ones). */
 int pkv_paged_decode_auto_partition(int num_seqs, int max_context, int block_size);
 
+/* Same decode for callers that cannot allocate device memory: code running where
+ * cudaMalloc is not allowed or not wanted (inside a caller-managed memory pool or
+ * arena with a fixed budget, a plugin whose host process owns every allocation, a
+ * real-time loop that must not touch the allocator).  The pages have no counterpart;
+ * this is a library convenience.  Arguments are those of pkv_paged_decode minus the
+ * workspace: the split-KV partials go to a scratch array built into the library
+ * (64 MiB, reserved on every GPU that loads libpkv's device code and held until the
+ * process exits).  The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *  - Its first call on a device looks up that device's copy of the scratch array
+ *    (with the device current); make that first call before any stream capture.
+ *  - Requests whose partials need more than 64 MiB
+ *    (pkv_paged_decode_workspace_bytes(...) > 64 MiB) return PKV_ERR_NOMEM before
+ *    any launch.
+ *  - Every call shares the one array, which keeps the last call's contents.  The
+ *    partials are fully written before they are read, so nothing needs clearing, but
+ *    calls whose kernels overlap on the GPU (other streams, other threads) race on
+ *    it: serialise them. */
+pkv_status pkv_paged_decode_noalloc(const pkv_pool_desc* pool, void* out, const void* q,
+                                    const void* k_pool, const void* v_pool,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int max_context, int num_seqs,
+                                    int num_q_heads, float scale, int partition_blocks,
+                                    void* stream);
+
 /* ---------------------------------------------------------------- paged_prefill
  * Causal prefill of new tokens over a cached prefix ("computes only the unseen
  * suffix" while reusing the cached prefix's K/V: aitalk.it, "RadixAttention: A Tree

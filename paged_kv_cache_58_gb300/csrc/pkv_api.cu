@@ -87,6 +87,30 @@ size_t decode_workspace(int num_seqs, int num_q_heads, int head_dim, int max_par
     return o + 2 * ml;
 }
 
+// Built-in decode scratch for pkv_paged_decode_noalloc: callers that cannot
+// allocate device memory get the split-KV partials here.  The array is reserved on
+// every GPU that loads this library's device code and held until the process exits.
+constexpr size_t kNoAllocScratchBytes = 64u << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device.  The host-side name
+// of a __device__ array is only a stand-in, so the address is looked up once per
+// device, with that device current, and cached; nullptr if the lookup fails.
+void* noalloc_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_scratch_addr[dev] = p;
+    }
+    return g_scratch_addr[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -208,6 +232,30 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
     if (pool->dtype == PKV_BF16 && !decode_use_simt())
         return from_cuda(pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_));
     return from_cuda(pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_));
+}
+
+pkv_status pkv_paged_decode_noalloc(const pkv_pool_desc* pool, void* out, const void* q,
+                                    const void* k_pool, const void* v_pool,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int max_context, int num_seqs,
+                                    int num_q_heads, float scale, int partition_blocks,
+                                    void* stream) {
+    pkv_status st = check_pool(pool);
+    if (st != PKV_OK) return st;
+    if (num_seqs < 0 || num_q_heads <= 0 || partition_blocks < 0 || max_context <= 0)
+        return PKV_ERR_INVALID;
+    if (num_seqs == 0) return PKV_OK;
+    const size_t need = pkv_paged_decode_workspace_bytes(
+        num_seqs, num_q_heads, pool->head_dim, max_context, pool->block_size, partition_blocks);
+    if (need > kNoAllocScratchBytes) return PKV_ERR_NOMEM;
+    void* scratch = nullptr;
+    if (need > 0) {
+        scratch = noalloc_scratch();
+        if (!scratch) return PKV_ERR_CUDA;
+    }
+    return pkv_paged_decode(pool, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                            context_lens, max_context, num_seqs, num_q_heads, scale,
+                            partition_blocks, scratch, need, stream);
 }
 
 pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q,
