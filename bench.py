@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--prefill-steps", type=int, default=20)
     p.add_argument("--min-warm-seconds", type=float, default=1.0,
                    help="warm-up also runs at least this long (clock sampling under load)")
     return p.parse_args()
@@ -56,13 +58,66 @@ def dist_env():
     return ws, rank, local
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
 def peaks():
+    """(hbm GB/s, bf16 burst TFLOP/s, kind) from MEASURED_PEAKS.json, else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         d = json.load(open(path))
-        return float(d["hbm_gbs"]), "measured"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def prefill_flops(case):
+    """Algorithmic flops of one prefill call: QK^T and PV over causal pairs only,
+    4 * D * Hq per (query token, key it attends)."""
+    D = case.q.shape[2]
+    Hq = case.q.shape[1]
+    total = 0
+    for c, n in zip(case.cached_lens.tolist(), case.new_lens.tolist()):
+        total += n * c + n * (n + 1) // 2     # sum over i < n of (c + i + 1)
+    return 4 * D * Hq * total
+
+
+def bench_prefill(pkv, dev, steps, stream):
+    """Prefix-cached chunked prefill (16 requests x 512 new tokens over cached
+    prefixes of U[1024, 8192]): kv_append of the new rows, then timed prefill calls
+    (CUDA events on the launching stream, K/V of 335 MB per call > L2)."""
+    import torch
+    import synth
+    case = synth.build_case("prefill", dev)
+    pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new,
+                  stream=stream)
+    out = torch.empty_like(case.q)
+    max_new = int(case.new_lens.max())
+
+    def call():
+        pkv.paged_prefill(case.q, case.k_pool, case.v_pool, case.block_tables,
+                          case.cached_lens, case.new_lens, case.q_offsets, case.scale,
+                          max_new=max_new, out=out, stream=stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    flops = prefill_flops(case)
+    kv_bytes = int((case.context_lens.to(torch.int64)).sum()) * case.k_pool.shape[1] * \
+        case.q.shape[2] * 2 * 2
+    res = {"workload": case.wl.name, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+           "flops_per_call": flops, "kv_bytes_per_call": kv_bytes, "launches": steps}
+    del case, out
+    return res
 
 
 class ClockSampler:
@@ -350,11 +405,17 @@ def main():
             dist.destroy_process_group()
         return
 
-    peak, peak_kind = peaks()
+    peak, tpeak, peak_kind = peaks()
     achieved = decode_bytes / (decode_ms * 1e-3) / 1e9
     traffic = kernel_traffic(os.path.join(ROOT, "paged_kv_cache_58_gb300", "csrc",
-                                          "paged_decode.cu"),
-                             os.path.join(ROOT, "profiles", "paged_decode_llama3_8b.md"))
+                                          "paged_decode_tc.cu"),
+                             os.path.join(ROOT, "profiles", "paged_decode_tc_llama3_8b.md"))
+    prefill = None
+    if not args.no_prefill:
+        prefill = bench_prefill(pkv, dev, args.prefill_steps, stream)
+        prefill.update({"bound": "tensor", "peak": tpeak, "unit": "TFLOP/s",
+                        "frac": prefill["tflops"] / tpeak,
+                        "peak_kind": f"{peak_kind} bf16_tflops (burst; kernel timed alone)"})
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -368,12 +429,13 @@ def main():
                    "kv_bytes_per_step": decode_bytes, "append_bytes_per_step": append_bytes,
                    "l2": "inputs larger than L2 (K/V read per step > 129 MB L2)",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode (split-KV + combine)",
+        "roofline": {"bound": "hbm", "kernel": "paged_decode (decode_tc split-KV + combine)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "decode_ms": decode_ms, "traffic": traffic},
         "e2e": e2e,
+        "prefill": prefill,
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }

@@ -9,25 +9,32 @@
 //
 // One CTA computes one 128-row query tile: TOK = 128 / G consecutive new tokens x
 // the G query heads that share kv head `kvh` (rows token-major, heads inner), so
-// every K/V tile it stages serves all G heads.  Per 128-key KV tile:
-//   S = Q K^T     tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) -> TMEM
-//   softmax       4 warps, one thread per row: tcgen05.ld S, causal mask, exp2,
-//                 row sums in fp32; P is split into bf16 hi + lo parts (P = hi + lo
-//                 to ~2^-17 relative) stored to TMEM with tcgen05.st
-//   O += P V      two tcgen05.mma passes (A = P hi, then P lo, read from TMEM; B = V
-//                 from shared memory) into a TMEM accumulator that lives across tiles
+// every K/V tile it stages serves all G heads.  Per 128-key KV tile j:
+//   S_j = Q K_j^T  tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) into TMEM
+//                  buffer j % 3
+//   softmax        4 warps, one thread per row: tcgen05.ld S_j, causal mask, exp2,
+//                  row sums in fp32; P_j is split into bf16 hi + lo parts (P = hi +
+//                  lo to ~2^-17 relative) and stored back over S_j in the same TMEM
+//                  buffer (hi in its first 64 columns, lo in the next 64)
+//   O += P_j V_j   two tcgen05.mma passes (A = P hi, then P lo, from TMEM; B = V_j
+//                  from shared memory) into a TMEM accumulator kept across tiles
 // The split keeps the probabilities at fp32-like precision: a single bf16 P is off by
 // up to 2^-9 per weight, which rows attending only a few keys do not average away.
 // The running max is updated lazily: O and l are rescaled only when a row's max
 // grows by more than 2^8, which keeps P <= 256 and leaves the result exact.
 //
-// Warp roles (192 threads): warps 0-3 softmax + epilogue (warp w owns TMEM lanes
-// 32w..32w+31), warp 4 TMA producer, warp 5 TMEM owner + MMA issuer.  K and V
-// tiles are double-buffered; each 16-token block of a tile arrives as two TMA
-// boxes (64 columns x 16 rows, 128-byte swizzle) per pool.
+// Pipelining.  The MMA issuer runs S_{j+1} before P_j V_j; S_{j+3} reuses the
+// buffer of P_j once P_j V_j has completed (its own per-buffer barrier: MMAs with
+// different accumulators are not ordered against each other), which with three
+// buffers is normally long done.  The softmax of tile j+1 overlaps P_j V_j and waits
+// for it only when a row's max grew (O rescale).  K stages (2) are released as soon as their S has
+// run, V stages (3) after their P.V, so the gathers of the next tiles are in flight
+// while the current one is computed.  Each 16-token block of a tile arrives as two
+// TMA boxes (64 columns x 16 rows, 128-byte swizzle) per pool.
 //
-// TMEM columns: S buffers at [0, 128) and [128, 256), O at [256, 384), P hi at
-// [384, 448) and P lo at [448, 512) (two bf16 per column).
+// Warp roles (192 threads): warps 0-3 softmax + epilogue (warp w owns TMEM lanes
+// 32w..32w+31), warp 4 TMA producer, warp 5 TMEM owner + MMA issuer.
+// TMEM columns: S/P buffers at [0, 128), [128, 256), [256, 384); O at [384, 512).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -46,20 +53,26 @@ constexpr int kBlk = 16;                   // tokens per pool block
 constexpr int kHalf = kRows * 128;         // one 64-column half of a 128-row tile: 16 KB
 constexpr int kTileBytes = 2 * kHalf;      // 32 KB
 constexpr int kBoxBytes = kBlk * 128;      // one TMA box: 16 rows x 128 B
-constexpr int kStages = 2;
+constexpr int kStagesK = 2;                // K stages: freed right after S = Q K^T
+constexpr int kStagesV = 3;                // V stages: freed after P.V
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
-constexpr int kNumBars = 12;
+constexpr int kOffV = kOffK + kStagesK * kTileBytes;
+constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
+constexpr int kNumBars = 20;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1 KB alignment slack
+constexpr int kSoftmaxWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 384;
+constexpr int kBufs = 3;                   // S/P buffers in TMEM
 constexpr float kLazyRescale = 8.0f;       // log2 units
 
 // barrier indices
-constexpr int BQ = 0, BKV_FULL = 1, BKV_EMPTY = 3, BS_FULL = 5, BS_FREE = 7, BP_FULL = 9,
-              BPV_DONE = 10;
+constexpr int BQ = 0, BK_FULL = 1, BK_EMPTY = 3, BV_FULL = 5, BV_EMPTY = 8, BS_FULL = 11,
+              BP_FULL = 14, BPV_DONE = 17;   // S_FULL / P_FULL / PV_DONE: one per buffer
 
 struct Ctl {
     uint64_t* bars;
@@ -129,17 +142,22 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     Ctl ctl{bars, abort_flag, a.status};
 
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         if (lane == 0) {
             mbar_init(&bars[BQ], 1);
-            for (int s = 0; s < kStages; ++s) {
-                mbar_init(&bars[BKV_FULL + s], 1);
-                mbar_init(&bars[BKV_EMPTY + s], 1);
-                mbar_init(&bars[BS_FULL + s], 1);
-                mbar_init(&bars[BS_FREE + s], 4);
+            for (int s = 0; s < kStagesK; ++s) {
+                mbar_init(&bars[BK_FULL + s], 1);
+                mbar_init(&bars[BK_EMPTY + s], 1);
             }
-            mbar_init(&bars[BP_FULL], 4);
-            mbar_init(&bars[BPV_DONE], 1);
+            for (int s = 0; s < kStagesV; ++s) {
+                mbar_init(&bars[BV_FULL + s], 1);
+                mbar_init(&bars[BV_EMPTY + s], 1);
+            }
+            for (int b = 0; b < kBufs; ++b) {
+                mbar_init(&bars[BS_FULL + b], 1);
+                mbar_init(&bars[BP_FULL + b], kSoftmaxWarps);
+                mbar_init(&bars[BPV_DONE + b], 1);
+            }
             *abort_flag = 0;
             fence_mbar_init();
         }
@@ -156,77 +174,108 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t sK = smem_u32(smem + kOffK);
     const uint32_t sV = smem_u32(smem + kOffV);
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
+        // The whole warp runs the loop: each lane prefetches one block id (32 ids =
+        // 4 KV tiles per refill, independent loads), lane 0 sets the byte counts and
+        // lane b < 8 issues the boxes of block b of the tile.
+        const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
+        const int nblk_needed = max_lim / kBlk + 1;
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
-            const int nblk_needed = max_lim / kBlk + 1;
             mbar_arrive_expect_tx(&bars[BQ], kTileBytes);
             tma_load_3d(smem + kOffQ, &tm_q, 0, kvh * G, qrow0, &bars[BQ]);
             tma_load_3d(smem + kOffQ + kHalf, &tm_q, 64, kvh * G, qrow0, &bars[BQ]);
-            for (int jt = 0; jt < ntiles; ++jt) {
-                const int s = jt & 1;
-                if (jt >= 2 && !wait_bar(ctl, BKV_EMPTY + s, ((jt >> 1) - 1) & 1)) break;
-                const int nb = min(kKeys / kBlk, nblk_needed - jt * (kKeys / kBlk));
-                mbar_arrive_expect_tx(&bars[BKV_FULL + s], nb * 4 * kBoxBytes);
-                uint8_t* kdst = smem + kOffK + s * kTileBytes;
-                uint8_t* vdst = smem + kOffV + s * kTileBytes;
-                for (int b = 0; b < nb; ++b) {
-                    int phys = __ldg(bt + jt * (kKeys / kBlk) + b);
-                    if (phys < 0 || phys >= a.num_blocks) {
-                        raise_status(a.status, PKV_ERR_OOB);
-                        phys = 0;  // keep the byte count; the output is flagged invalid
-                    }
-                    const int row = (phys * a.num_kv_heads + kvh) * kBlk;
-                    tma_load_2d(kdst + b * kBoxBytes, &tm_k, 0, row, &bars[BKV_FULL + s]);
-                    tma_load_2d(kdst + kHalf + b * kBoxBytes, &tm_k, 64, row,
-                                &bars[BKV_FULL + s]);
-                    tma_load_2d(vdst + b * kBoxBytes, &tm_v, 0, row, &bars[BKV_FULL + s]);
-                    tma_load_2d(vdst + kHalf + b * kBoxBytes, &tm_v, 64, row,
-                                &bars[BKV_FULL + s]);
-                }
-            }
         }
-    } else if (warp == 5) {
+        int ids = 0;
+        for (int jt = 0; jt < ntiles; ++jt) {
+            constexpr int kPerTile = kKeys / kBlk;   // 8 blocks per KV tile
+            if ((jt & 3) == 0) {
+                const int i = jt * kPerTile + lane;
+                ids = (i < nblk_needed) ? __ldg(bt + i) : 0;
+            }
+            const int sk = jt % kStagesK;
+            const int sv = jt % kStagesV;
+            const int nb = min(kPerTile, nblk_needed - jt * kPerTile);
+            int phys = __shfl_sync(0xffffffffu, ids, ((jt & 3) * kPerTile) + (lane & 7));
+            if (phys < 0 || phys >= a.num_blocks) {
+                if (lane < nb) raise_status(a.status, PKV_ERR_OOB);
+                phys = 0;  // keep the byte count; the output is flagged invalid
+            }
+            const int row = (phys * a.num_kv_heads + kvh) * kBlk;
+            // K of tile jt: its stage is free once S of tile jt - kStagesK has run.
+            int ok = 1;
+            if (lane == 0 && jt >= kStagesK)
+                ok = wait_bar(ctl, BK_EMPTY + sk, ((jt / kStagesK) - 1) & 1);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&bars[BK_FULL + sk], nb * 2 * kBoxBytes);
+            __syncwarp();
+            if (lane < nb) {
+                uint8_t* kdst = smem + kOffK + sk * kTileBytes + lane * kBoxBytes;
+                tma_load_2d(kdst, &tm_k, 0, row, &bars[BK_FULL + sk]);
+                tma_load_2d(kdst + kHalf, &tm_k, 64, row, &bars[BK_FULL + sk]);
+            }
+            // V of tile jt: its stage is free once P.V of tile jt - kStagesV has run.
+            if (lane == 0 && jt >= kStagesV)
+                ok = wait_bar(ctl, BV_EMPTY + sv, ((jt / kStagesV) - 1) & 1);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&bars[BV_FULL + sv], nb * 2 * kBoxBytes);
+            __syncwarp();
+            if (lane < nb) {
+                uint8_t* vdst = smem + kOffV + sv * kTileBytes + lane * kBoxBytes;
+                tma_load_2d(vdst, &tm_v, 0, row, &bars[BV_FULL + sv]);
+                tma_load_2d(vdst + kHalf, &tm_v, 64, row, &bars[BV_FULL + sv]);
+            }
+            __syncwarp();
+        }
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, kKeys, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, kHead, false, true);
-            const uint32_t tO = tmem + 256;
+            const uint32_t tO = tmem + kTmemO;
             bool ok = wait_bar(ctl, BQ, 0);
             for (int jt = 0; ok && jt <= ntiles; ++jt) {
                 if (jt < ntiles) {
-                    const int s = jt & 1;
-                    if (!wait_bar(ctl, BKV_FULL + s, (jt >> 1) & 1)) break;
-                    if (jt >= 2 && !wait_bar(ctl, BS_FREE + s, ((jt >> 1) - 1) & 1)) break;
+                    // S_jt into buffer jt % 3, once P_{jt-3} in it has been consumed.
+                    const int ks_ = jt % kStagesK;
+                    const int sb = jt % kBufs;
+                    if (!wait_bar(ctl, BK_FULL + ks_, (jt / kStagesK) & 1)) break;
+                    if (jt >= kBufs && !wait_bar(ctl, BPV_DONE + sb, ((jt / kBufs) - 1) & 1))
+                        break;
                     tc_fence_after();
-                    const uint32_t tS = tmem + s * 128;
+                    const uint32_t tS = tmem + sb * 128;
 #pragma unroll
                     for (int ks = 0; ks < kHead / 16; ++ks) {
                         const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
                         umma_bf16(tS, smem_desc_sw128(sQ + off, 16, 1024),
-                                  smem_desc_sw128(sK + s * kTileBytes + off, 16, 1024), idesc_qk,
-                                  ks > 0);
+                                  smem_desc_sw128(sK + ks_ * kTileBytes + off, 16, 1024),
+                                  idesc_qk, ks > 0);
                     }
-                    umma_commit(&bars[BS_FULL + s]);
+                    umma_commit(&bars[BS_FULL + sb]);
+                    umma_commit(&bars[BK_EMPTY + ks_]);
                 }
                 if (jt >= 1) {
                     const int j = jt - 1;
-                    const int sj = j & 1;
-                    if (!wait_bar(ctl, BP_FULL, j & 1)) break;
+                    const int pb = j % kBufs;
+                    const int vs = j % kStagesV;
+                    if (!wait_bar(ctl, BP_FULL + pb, (j / kBufs) & 1)) break;
+                    if (!wait_bar(ctl, BV_FULL + vs, (j / kStagesV) & 1)) break;
                     tc_fence_after();
+                    const uint32_t tP = tmem + pb * 128;
 #pragma unroll
                     for (int ks = 0; ks < kKeys / 16; ++ks) {
                         const uint64_t bv =
-                            smem_desc_sw128(sV + sj * kTileBytes + ks * 2048, kHalf, 1024);
-                        umma_bf16_ta(tO, tmem + 384 + ks * 8, bv, idesc_pv, (j > 0) || (ks > 0));
-                        umma_bf16_ta(tO, tmem + 448 + ks * 8, bv, idesc_pv, true);
+                            smem_desc_sw128(sV + vs * kTileBytes + ks * 2048, kHalf, 1024);
+                        umma_bf16_ta(tO, tP + ks * 8, bv, idesc_pv, (j > 0) || (ks > 0));
+                        umma_bf16_ta(tO, tP + 64 + ks * 8, bv, idesc_pv, true);
                     }
-                    umma_commit(&bars[BPV_DONE]);
-                    umma_commit(&bars[BKV_EMPTY + sj]);
+                    umma_commit(&bars[BPV_DONE + pb]);
+                    umma_commit(&bars[BV_EMPTY + vs]);
                 }
             }
         }
@@ -243,98 +292,113 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         float l = 0.f;
         bool ok = true;
         for (int jt = 0; jt < ntiles; ++jt) {
-            const int s = jt & 1;
-            if (!wait_bar_warp(ctl, BS_FULL + s, (jt >> 1) & 1, lane)) { ok = false; break; }
+            const int b = jt % kBufs;
+            const uint32_t tS = tmem + lane_addr + b * 128;
+            if (!wait_bar_warp(ctl, BS_FULL + b, (jt / kBufs) & 1, lane)) { ok = false; break; }
             tc_fence_after();
             float x[kKeys];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                tmem_ld32(tmem + lane_addr + s * 128 + q * 32,
-                          *reinterpret_cast<float(*)[32]>(&x[q * 32]));
+                tmem_ld32(tS + q * 32, *reinterpret_cast<float(*)[32]>(&x[q * 32]));
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[BS_FREE + s]);
 
             const int kbase = jt * kKeys;
-            float mx = -INFINITY;
+            // Row max over 8 independent chains (one softmax warp per scheduler has
+            // no other warp to hide long dependency chains behind).
+            float m8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
             if (kbase + kKeys - 1 <= lim) {
 #pragma unroll
-                for (int k = 0; k < kKeys; ++k) mx = fmaxf(mx, x[k]);
+                for (int k = 0; k < kKeys; ++k) m8[k & 7] = fmaxf(m8[k & 7], x[k]);
             } else {
 #pragma unroll
                 for (int k = 0; k < kKeys; ++k) {
                     x[k] = (kbase + k <= lim) ? x[k] : -INFINITY;
-                    mx = fmaxf(mx, x[k]);
+                    m8[k & 7] = fmaxf(m8[k & 7], x[k]);
                 }
             }
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             const float m_tile = mx * sl2;   // scale > 0: max commutes with scaling
             const bool grow = m_tile > m_used + kLazyRescale;
             const float m_cur = grow ? m_tile : m_used;
             const float alpha = fast_exp2(m_used - m_cur);   // 1 unless grow; 0 at start
-            float rs = 0.f;
+            float rs8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
             float phi[kKeys / 2], plo[kKeys / 2];   // packed bf16 pairs, as fp32 bit patterns
 #pragma unroll
             for (int k = 0; k < kKeys; k += 2) {
                 const float p0 = fast_exp2(fmaf(x[k], sl2, -m_cur));
                 const float p1 = fast_exp2(fmaf(x[k + 1], sl2, -m_cur));
-                rs += p0 + p1;
+                rs8[(k >> 1) & 7] += p0 + p1;
                 const uint32_t h = pack_bf16x2(p0, p1);
                 const float r0 = p0 - bf16lo_to_f32(h);
                 const float r1 = p1 - bf16hi_to_f32(h);
                 phi[k / 2] = __uint_as_float(h);
                 plo[k / 2] = __uint_as_float(pack_bf16x2(r0, r1));
             }
+            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
+                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             l = l * alpha + rs;
             m_used = m_cur;
 
-            // P and O may be touched only after the previous tile's P.V finished.
-            if (jt >= 1 && !wait_bar_warp(ctl, BPV_DONE, (jt - 1) & 1, lane)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
+            // O is rescaled only when some row of the warp grew its max; that needs the
+            // previous tile's P.V to have finished.  Otherwise P.V of tile jt - 1 keeps
+            // running while this tile's P is written to the other buffer.
             if (jt >= 1 && __any_sync(0xffffffffu, grow)) {
+                if (!wait_bar_warp(ctl, BPV_DONE + (jt - 1) % kBufs, ((jt - 1) / kBufs) & 1,
+                                   lane)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float o[32];
-                    const uint32_t ta = tmem + lane_addr + 256 + q * 32;
+                    const uint32_t ta = tmem + lane_addr + kTmemO + q * 32;
                     tmem_ld32(ta, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= alpha;
                     tmem_st32(ta, o);
                 }
-                tmem_wait_st();
             }
-            // P row -> TMEM (this thread's lane), hi and lo parts.
+            // P_jt over S_jt in the same buffer: hi in columns [0, 64), lo in [64, 128).
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                tmem_st32(tmem + lane_addr + 384 + q * 32,
-                          *reinterpret_cast<float(*)[32]>(&phi[q * 32]));
-                tmem_st32(tmem + lane_addr + 448 + q * 32,
-                          *reinterpret_cast<float(*)[32]>(&plo[q * 32]));
+                tmem_st32(tS + q * 32, *reinterpret_cast<float(*)[32]>(&phi[q * 32]));
+                tmem_st32(tS + 64 + q * 32, *reinterpret_cast<float(*)[32]>(&plo[q * 32]));
             }
             tmem_wait_st();
             // Keys past the last one this tile needs are masked for every row, but their
             // V rows may hold anything (NaN in unused slots, stale data where no block was
-            // loaded this tile); zero them so that 0 * V stays 0 in the P.V product.
-            if (kbase + row > max_lim) {
-                uint8_t* vrow = smem + kOffV + s * kTileBytes + row * 128;
-                const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    *reinterpret_cast<uint4*>(vrow + (j << 4)) = z;
-                    *reinterpret_cast<uint4*>(vrow + kHalf + (j << 4)) = z;
+            // loaded this tile); zero them so that 0 * V stays 0 in the P.V product, once
+            // this tile's V has landed.
+            if (kbase + kKeys - 1 > max_lim) {
+                if (!wait_bar_warp(ctl, BV_FULL + jt % kStagesV, (jt / kStagesV) & 1, lane)) {
+                    ok = false;
+                    break;
                 }
+                if (kbase + row > max_lim) {
+                    uint8_t* vrow = smem + kOffV + (jt % kStagesV) * kTileBytes + row * 128;
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        *reinterpret_cast<uint4*>(vrow + (j << 4)) = z;
+                        *reinterpret_cast<uint4*>(vrow + kHalf + (j << 4)) = z;
+                    }
+                }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[BP_FULL]);
+            if (lane == 0) mbar_arrive(&bars[BP_FULL + b]);
         }
         // ------------------------------------------------------------ epilogue
-        if (ok && wait_bar_warp(ctl, BPV_DONE, (ntiles - 1) & 1, lane)) {
+        if (ok && wait_bar_warp(ctl, BPV_DONE + (ntiles - 1) % kBufs,
+                                ((ntiles - 1) / kBufs) & 1, lane)) {
             tc_fence_after();
             const float inv_l = 1.f / l;
             uint16_t* orow = static_cast<uint16_t*>(a.out) +
@@ -343,7 +407,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float o[32];
-                tmem_ld32(tmem + lane_addr + 256 + q * 32, o);
+                tmem_ld32(tmem + lane_addr + kTmemO + q * 32, o);
                 tmem_wait_ld();
                 if (row_valid) {
 #pragma unroll
@@ -362,7 +426,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
