@@ -126,6 +126,16 @@ PKV_DEVINL void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before its predecessor on the stream finishes;
+// griddep_wait() blocks until that predecessor has completed and its writes are
+// visible (a no-op otherwise).  griddep_launch_dependents() lets the next such
+// kernel be scheduled early.
+PKV_DEVINL void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+PKV_DEVINL void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 PKV_DEVINL float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

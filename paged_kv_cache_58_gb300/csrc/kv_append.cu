@@ -25,6 +25,8 @@ kv_append_kernel(uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
                  const uint8_t* __restrict__ v, int64_t num_chunks, int chunks_per_row,
                  int num_kv_heads, int row_bytes, int block_size, int64_t num_slots,
                  int* status) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= num_chunks) return;
     const int chunk = static_cast<int>(idx % chunks_per_row);
@@ -52,6 +54,8 @@ __global__ void __launch_bounds__(256)
 copy_blocks_kernel(uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
                    const int32_t* __restrict__ pairs, int64_t block_bytes, int64_t num_blocks,
                    int* status) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int src = __ldg(pairs + 2 * blockIdx.x);
     const int dst = __ldg(pairs + 2 * blockIdx.x + 1);
     if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
@@ -75,21 +79,20 @@ cudaError_t launch_kv_append(void* k_pool, void* v_pool, const int64_t* slot_map
     const int64_t num_chunks = num_tokens * num_kv_heads * chunks_per_row;
     if (num_chunks == 0) return cudaSuccess;
     const int64_t grid = (num_chunks + 255) / 256;
-    kv_append_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-        static_cast<uint8_t*>(k_pool), static_cast<uint8_t*>(v_pool), slot_mapping,
-        static_cast<const uint8_t*>(k), static_cast<const uint8_t*>(v), num_chunks,
-        chunks_per_row, num_kv_heads, row_bytes, block_size, num_blocks * block_size, status);
-    return cudaGetLastError();
+    return launch_pdl(kv_append_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream,
+                      static_cast<uint8_t*>(k_pool), static_cast<uint8_t*>(v_pool), slot_mapping,
+                      static_cast<const uint8_t*>(k), static_cast<const uint8_t*>(v), num_chunks,
+                      chunks_per_row, num_kv_heads, row_bytes, block_size,
+                      num_blocks * block_size, status);
 }
 
 cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs,
                                int64_t block_bytes, int64_t num_blocks, int* status,
                                cudaStream_t stream) {
     if (num_pairs == 0) return cudaSuccess;
-    copy_blocks_kernel<<<dim3(num_pairs, 2), 256, 0, stream>>>(
-        static_cast<uint8_t*>(k_pool), static_cast<uint8_t*>(v_pool), pairs, block_bytes,
-        num_blocks, status);
-    return cudaGetLastError();
+    return launch_pdl(copy_blocks_kernel, dim3(num_pairs, 2), dim3(256), 0, stream,
+                      static_cast<uint8_t*>(k_pool), static_cast<uint8_t*>(v_pool), pairs,
+                      block_bytes, num_blocks, status);
 }
 
 }  // namespace pkv

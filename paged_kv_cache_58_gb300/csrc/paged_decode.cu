@@ -139,6 +139,8 @@ decode_split_kernel(const DecodeArgs a) {
     constexpr int NE = D / 16;
     extern __shared__ __align__(128) uint8_t smem[];
 
+    griddep_wait();
+    griddep_launch_dependents();
     const int part = blockIdx.x;
     const int kvh = blockIdx.y;
     const int seq = blockIdx.z;
@@ -363,60 +365,75 @@ decode_split_kernel(const DecodeArgs a) {
 
 // Log-sum-exp merge of the partitions of one (sequence, query head):
 // M = max m_p, w_p = l_p * 2^(m_p - M), out = sum w_p o_p / sum w_p.
+// One warp per (sequence, query head); lane i owns elements [i*D/32, (i+1)*D/32)
+// and the partials of all partitions are loaded 8 at a time so their latencies
+// overlap.
+constexpr int kCombineWarps = 4;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(kCombineWarps * 32)
 decode_combine_kernel(const DecodeArgs a) {
-    __shared__ float wsm[kMaxParts];
-    __shared__ float red[D / 32];
-    const int h = blockIdx.x;
-    const int seq = blockIdx.y;
-    const int d = threadIdx.x;
+    griddep_wait();
+    griddep_launch_dependents();
+    constexpr int EL = D / 32;  // 4 (D 128) or 2 (D 64) elements per lane
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const size_t row = static_cast<size_t>(blockIdx.x) * kCombineWarps + warp;  // seq*Hq + h
+    if (row >= static_cast<size_t>(a.num_seqs) * a.num_q_heads) return;
+    const int seq = static_cast<int>(row / a.num_q_heads);
     const int L = min(a.context_lens[seq], a.max_blocks_per_seq * kBlock);
     const int nblk = (L + kBlock - 1) / kBlock;
     const int np = min(a.max_parts, (nblk + a.partition_blocks - 1) / a.partition_blocks);
     if (np <= 0) return;
-    const size_t row = static_cast<size_t>(seq) * a.num_q_heads + h;
     const float* mp = a.m_part + row * a.max_parts;
     const float* lp = a.l_part + row * a.max_parts;
 
     float M = -INFINITY;
-    for (int p = d; p < np; p += D) M = fmaxf(M, mp[p]);
+    for (int p = lane; p < np; p += 32) M = fmaxf(M, mp[p]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if ((d & 31) == 0) red[d >> 5] = M;
-    __syncthreads();
-    M = red[0];
-#pragma unroll
-    for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
-    __syncthreads();
 
+    const float* op = a.o_part + row * a.max_parts * D + lane * EL;
+    float acc[EL];
+#pragma unroll
+    for (int e = 0; e < EL; ++e) acc[e] = 0.f;
     float W = 0.f;
-    for (int p = d; p < np; p += D) {
-        const float w = lp[p] * fast_exp2(mp[p] - M);
-        wsm[p] = w;
+    for (int base = 0; base < np; base += 32) {
+        const int p = base + lane;
+        const float w = (p < np) ? lp[p] * fast_exp2(mp[p] - M) : 0.f;
         W += w;
+        const int cnt = min(32, np - base);
+        for (int u0 = 0; u0 < cnt; u0 += 8) {
+            float v[8][EL];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (u0 + u < cnt) {
+                    const float* src = op + static_cast<size_t>(base + u0 + u) * D;
+                    if constexpr (EL == 4) {
+                        const float4 f = *reinterpret_cast<const float4*>(src);
+                        v[u][0] = f.x; v[u][1] = f.y; v[u][2] = f.z; v[u][3] = f.w;
+                    } else {
+                        const float2 f = *reinterpret_cast<const float2*>(src);
+                        v[u][0] = f.x; v[u][1] = f.y;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float wu = __shfl_sync(0xffffffffu, w, (u0 + u) & 31);
+                if (u0 + u < cnt) {
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) acc[e] = fmaf(wu, v[u][e], acc[e]);
+                }
+            }
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
-    if ((d & 31) == 0) red[d >> 5] = W;
-    __syncthreads();
-    W = 0.f;
+    const float inv = 1.f / W;
+    T* dst = static_cast<T*>(a.out) + row * D + lane * EL;
 #pragma unroll
-    for (int w = 0; w < D / 32; ++w) W += red[w];
-
-    // Independent loads, 8 partitions at a time, so the partial reads overlap.
-    const float* op = a.o_part + row * a.max_parts * D + d;
-    float acc = 0.f;
-    int p = 0;
-    for (; p + 8 <= np; p += 8) {
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldg(op + static_cast<size_t>(p + u) * D);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) acc = fmaf(wsm[p + u], v[u], acc);
-    }
-    for (; p < np; ++p) acc = fmaf(wsm[p], __ldg(op + static_cast<size_t>(p) * D), acc);
-    store_elem<T>(static_cast<T*>(a.out) + row * D + d, acc / W);
+    for (int e = 0; e < EL; ++e) store_elem<T>(dst + e, acc[e] * inv);
 }
 
 template <typename T, int D, int G>
@@ -427,17 +444,17 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
                                          SM::kTotal);
     if (e != cudaSuccess) return e;
     dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
-    kern<<<grid, kThreads, SM::kTotal, stream>>>(a);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, grid, dim3(kThreads), SM::kTotal, stream, a);
     if (e != cudaSuccess || a.max_parts == 1) return e;
-    decode_combine_kernel<T, D><<<dim3(a.num_q_heads, a.num_seqs), D, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_decode_combine(a, sizeof(T) == 2 ? PKV_BF16 : PKV_F32, D, stream);
 }
 
 template <typename T, int D>
 cudaError_t launch_combine_typed(const DecodeArgs& a, cudaStream_t stream) {
-    decode_combine_kernel<T, D><<<dim3(a.num_q_heads, a.num_seqs), D, 0, stream>>>(a);
-    return cudaGetLastError();
+    const size_t rows = static_cast<size_t>(a.num_seqs) * a.num_q_heads;
+    const unsigned grid = static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps);
+    return launch_pdl(decode_combine_kernel<T, D>, dim3(grid), dim3(kCombineWarps * 32), 0,
+                      stream, a);
 }
 
 template <typename T, int D>

@@ -92,6 +92,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
+    griddep_wait();
+    griddep_launch_dependents();
     const int part = blockIdx.x;
     const int kvh = blockIdx.y;
     const int seq = blockIdx.z;
@@ -359,8 +361,7 @@ cudaError_t launch_tc(const DecodeArgs& a, cudaStream_t stream) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
     if (e != cudaSuccess) return e;
     dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
-    kern<<<grid, kThreads, SM::kTotal, stream>>>(mk, mv, a);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, grid, dim3(kThreads), SM::kTotal, stream, mk, mv, a);
     if (e != cudaSuccess || a.max_parts == 1) return e;
     return launch_decode_combine(a, PKV_BF16, D, stream);
 }

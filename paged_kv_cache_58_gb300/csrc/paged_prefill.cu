@@ -27,7 +27,7 @@
 // buffer of P_j once P_j V_j has completed (its own per-buffer barrier: MMAs with
 // different accumulators are not ordered against each other), which with three
 // buffers is normally long done.  The softmax of tile j+1 overlaps P_j V_j and waits
-// for it only when a row's max grew (O rescale).  K stages (2) are released as soon as their S has
+// for it only when a row's max grew (O rescale).  K stages (3) are released as soon as their S has
 // run, V stages (3) after their P.V, so the gathers of the next tiles are in flight
 // while the current one is computed.  Each 16-token block of a tile arrives as two
 // TMA boxes (64 columns x 16 rows, 128-byte swizzle) per pool.
@@ -53,13 +53,13 @@ constexpr int kBlk = 16;                   // tokens per pool block
 constexpr int kHalf = kRows * 128;         // one 64-column half of a 128-row tile: 16 KB
 constexpr int kTileBytes = 2 * kHalf;      // 32 KB
 constexpr int kBoxBytes = kBlk * 128;      // one TMA box: 16 rows x 128 B
-constexpr int kStagesK = 2;                // K stages: freed right after S = Q K^T
+constexpr int kStagesK = 3;                // K stages: freed right after S = Q K^T
 constexpr int kStagesV = 3;                // V stages: freed after P.V
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileBytes;
 constexpr int kOffV = kOffK + kStagesK * kTileBytes;
 constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
-constexpr int kNumBars = 20;
+constexpr int kNumBars = 24;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1 KB alignment slack
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
@@ -71,8 +71,8 @@ constexpr int kBufs = 3;                   // S/P buffers in TMEM
 constexpr float kLazyRescale = 8.0f;       // log2 units
 
 // barrier indices
-constexpr int BQ = 0, BK_FULL = 1, BK_EMPTY = 3, BV_FULL = 5, BV_EMPTY = 8, BS_FULL = 11,
-              BP_FULL = 14, BPV_DONE = 17;   // S_FULL / P_FULL / PV_DONE: one per buffer
+constexpr int BQ = 0, BK_FULL = 1, BK_EMPTY = 4, BV_FULL = 7, BV_EMPTY = 10, BS_FULL = 13,
+              BP_FULL = 16, BPV_DONE = 19;   // S_FULL / P_FULL / PV_DONE: one per buffer
 
 struct Ctl {
     uint64_t* bars;
@@ -117,6 +117,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
+    griddep_wait();
+    griddep_launch_dependents();
     const int qt = blockIdx.x;
     const int kvh = blockIdx.y;
     const int r = blockIdx.z;
@@ -324,29 +326,9 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             const bool grow = m_tile > m_used + kLazyRescale;
             const float m_cur = grow ? m_tile : m_used;
             const float alpha = fast_exp2(m_used - m_cur);   // 1 unless grow; 0 at start
-            float rs8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
-            float phi[kKeys / 2], plo[kKeys / 2];   // packed bf16 pairs, as fp32 bit patterns
-#pragma unroll
-            for (int k = 0; k < kKeys; k += 2) {
-                const float p0 = fast_exp2(fmaf(x[k], sl2, -m_cur));
-                const float p1 = fast_exp2(fmaf(x[k + 1], sl2, -m_cur));
-                rs8[(k >> 1) & 7] += p0 + p1;
-                const uint32_t h = pack_bf16x2(p0, p1);
-                const float r0 = p0 - bf16lo_to_f32(h);
-                const float r1 = p1 - bf16hi_to_f32(h);
-                phi[k / 2] = __uint_as_float(h);
-                plo[k / 2] = __uint_as_float(pack_bf16x2(r0, r1));
-            }
-            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
-                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-            l = l * alpha + rs;
-            m_used = m_cur;
-
             // O is rescaled only when some row of the warp grew its max; that needs the
             // previous tile's P.V to have finished.  Otherwise P.V of tile jt - 1 keeps
-            // running while this tile's P is written to the other buffer.
+            // running while this tile's P is written to its own buffer.
             if (jt >= 1 && __any_sync(0xffffffffu, grow)) {
                 if (!wait_bar_warp(ctl, BPV_DONE + (jt - 1) % kBufs, ((jt - 1) / kBufs) & 1,
                                    lane)) {
@@ -365,12 +347,32 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                     tmem_st32(ta, o);
                 }
             }
-            // P_jt over S_jt in the same buffer: hi in columns [0, 64), lo in [64, 128).
+            // P_jt over S_jt in the same buffer (S is already in registers): hi in columns
+            // [0, 64), lo in [64, 128), written 32 keys at a time so that few packed
+            // values are live and the exp chains of a chunk overlap.
+            float rs8[8];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                tmem_st32(tS + q * 32, *reinterpret_cast<float(*)[32]>(&phi[q * 32]));
-                tmem_st32(tS + 64 + q * 32, *reinterpret_cast<float(*)[32]>(&plo[q * 32]));
+            for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+#pragma unroll
+            for (int q = 0; q < kKeys / 32; ++q) {
+                uint32_t phi[16], plo[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int k = q * 32 + 2 * e;
+                    const float p0 = fast_exp2(fmaf(x[k], sl2, -m_cur));
+                    const float p1 = fast_exp2(fmaf(x[k + 1], sl2, -m_cur));
+                    rs8[e & 7] += p0 + p1;
+                    const uint32_t h = pack_bf16x2(p0, p1);
+                    phi[e] = h;
+                    plo[e] = pack_bf16x2(p0 - bf16lo_to_f32(h), p1 - bf16hi_to_f32(h));
+                }
+                tmem_st16(tS + q * 16, phi);
+                tmem_st16(tS + 64 + q * 16, plo);
             }
+            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
+                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+            l = l * alpha + rs;
+            m_used = m_cur;
             tmem_wait_st();
             // Keys past the last one this tile needs are masked for every row, but their
             // V rows may hold anything (NaN in unused slots, stale data where no block was
@@ -446,8 +448,7 @@ cudaError_t launch_g(const PrefillArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     constexpr int TOK = kRows / G;
     dim3 grid((a.max_new + TOK - 1) / TOK, a.num_kv_heads, a.num_reqs);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, stream, mq, mk, mv, a);
 }
 
 }  // namespace
