@@ -27,10 +27,14 @@
 // buffer of P_j once P_j V_j has completed (its own per-buffer barrier: MMAs with
 // different accumulators are not ordered against each other), which with three
 // buffers is normally long done.  The softmax of tile j+1 overlaps P_j V_j and waits
-// for it only when a row's max grew (O rescale).  K stages (3) are released as soon as their S has
-// run, V stages (3) after their P.V, so the gathers of the next tiles are in flight
-// while the current one is computed.  Each 16-token block of a tile arrives as two
-// TMA boxes (64 columns x 16 rows, 128-byte swizzle) per pool.
+// for it only when a row's max grew (O rescale).  K stages (3) are released as soon
+// as their S has run, V stages (3) after their P.V, so the gathers of the next tiles
+// are in flight while the current one is computed.  Each 16-token block of a tile
+// arrives as two TMA boxes (64 columns x 16 rows, 128-byte swizzle) per pool.
+//
+// Measured limit: a 128 x 128 x 16 tcgen05.mma issues in about the time of a
+// 128 x 256 x 16 one, so the 24 N = 128 MMAs per tile (8 for S, 16 for the hi + lo
+// P.V) set the pace; the softmax finishes inside that time.
 //
 // Warp roles (192 threads): warps 0-3 softmax + epilogue (warp w owns TMEM lanes
 // 32w..32w+31), warp 4 TMA producer, warp 5 TMEM owner + MMA issuer.
