@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode HBM GB/s (% of ~8 TB/s peak) and decode tokens/s per layer"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-WORKLOAD = "8b"
+DECODE_WORKLOADS = ("8b", "70b", "shared", "tiny")
 
 
 def parse():
@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--workload", choices=DECODE_WORKLOADS, default="8b",
+                   help="decode workload of the step (default: the Llama-3-8B-shaped batch)")
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--prefill-steps", type=int, default=20)
     p.add_argument("--min-warm-seconds", type=float, default=1.0,
@@ -208,7 +210,7 @@ def run_reference(args, ws, rank):
     import oracle
     import synth
     oracle.build()
-    case = synth.build_case(WORKLOAD, "cpu")
+    case = synth.build_case(args.workload, "cpu")
     decode_bytes, append_bytes, tokens = workload_bytes(case)
     kp, vp = synth.host_bits(case.k_pool), synth.host_bits(case.v_pool)
     q, bt = synth.host_bits(case.q), synth.host_bits(case.block_tables)
@@ -296,7 +298,7 @@ def main():
     if ws > 1:
         dist.barrier()
 
-    case = synth.build_case(WORKLOAD, dev)
+    case = synth.build_case(args.workload, dev)
     S, Hq, D = case.q.shape
     decode_bytes, append_bytes, tokens = workload_bytes(case)
     max_ctx = case.max_context
@@ -407,9 +409,11 @@ def main():
 
     peak, tpeak, peak_kind = peaks()
     achieved = decode_bytes / (decode_ms * 1e-3) / 1e9
-    traffic = kernel_traffic(os.path.join(ROOT, "paged_kv_cache_58_gb300", "csrc",
-                                          "paged_decode_tc.cu"),
-                             os.path.join(ROOT, "profiles", "paged_decode_tc_llama3_8b.md"))
+    traffic = None
+    if args.workload == "8b" and case.q.dtype.itemsize == 2:
+        traffic = kernel_traffic(os.path.join(ROOT, "paged_kv_cache_58_gb300", "csrc",
+                                              "paged_decode_tc.cu"),
+                                 os.path.join(ROOT, "profiles", "paged_decode_tc_llama3_8b.md"))
     prefill = None
     if not args.no_prefill:
         prefill = bench_prefill(pkv, dev, args.prefill_steps, stream)
@@ -427,7 +431,9 @@ def main():
                    "pool_blocks": case.k_pool.shape[0], "mean_context": tokens / S,
                    "max_context": max_ctx, "partition_blocks": pb,
                    "kv_bytes_per_step": decode_bytes, "append_bytes_per_step": append_bytes,
-                   "l2": "inputs larger than L2 (K/V read per step > 129 MB L2)",
+                   "l2": ("inputs larger than L2 (K/V read per step > 129 MB L2)"
+                          if decode_bytes > 2 * 129e6 else
+                          "K/V per step smaller than L2: warm-cache figure"),
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"bound": "hbm", "kernel": "paged_decode (decode_tc split-KV + combine)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -1,6 +1,9 @@
 """Shared test helpers: oracle runs on seeded cases and the tolerance check."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -37,6 +40,14 @@ def check_attention(got: torch.Tensor, ref: np.ndarray, mask: np.ndarray | None 
     bad = (err > ATOL) & (err > RTOL * np.abs(ref))
     max_abs = float(err.max())
     score = float((err / np.maximum(np.abs(ref), ATOL / RTOL)).max())
+    log = os.environ.get("PKV_PARITY_LOG")
+    if log:   # optional record of the errors, for reports
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "?"),
+                                "elements": int(err.size), "max_abs": max_abs,
+                                "max_rel_floored": score,
+                                "max_rel": float((err / np.maximum(np.abs(ref), 1e-30)).max()),
+                                "outside": int(bad.sum())}) + "\n")
     if bad.any():
         i = np.unravel_index(np.argmax(np.where(bad, err, 0)), err.shape)
         raise AssertionError(f"{int(bad.sum())} of {err.size} elements outside both bounds; "
