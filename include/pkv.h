@@ -227,10 +227,79 @@ pkv_status pkv_alloc_free_seq(pkv_alloc* a, int64_t seq_id);
 pkv_status pkv_alloc_block_table(const pkv_alloc* a, const int64_t* seq_ids, int num_seqs,
                                  int32_t* out, int max_blocks);
 
+/* Registers seq_id holding num_tokens tokens whose first num_shared blocks are the given
+ * existing blocks (refcount + 1 each), e.g. a prefix found by pkv_pcache_match or
+ * pkv_radix_match; the remaining ceil(num_tokens / B) - num_shared blocks are new.  The
+ * last shared block may be partially filled (num_tokens < num_shared * B): the next
+ * pkv_alloc_append then copies it first (copy-on-write).  PKV_ERR_INVALID if a block is
+ * not allocated or num_shared exceeds the blocks num_tokens needs. */
+pkv_status pkv_alloc_add_seq_shared(pkv_alloc* a, int64_t seq_id, const int32_t* shared_blocks,
+                                    int num_shared, int64_t num_tokens);
+
 int64_t pkv_alloc_num_free(const pkv_alloc* a);
 int pkv_alloc_refcount(const pkv_alloc* a, int64_t block);            /* -1 if out of range */
 int64_t pkv_alloc_seq_len(const pkv_alloc* a, int64_t seq_id);        /* -1 if unknown */
 int64_t pkv_alloc_seq_num_blocks(const pkv_alloc* a, int64_t seq_id); /* -1 if unknown */
+
+/* ---------------------------------------------------------------- prefix reuse: block hashes
+ * Chained block hashes (aitalk.it, "Two Layers, Not Two Rivals": each completed block is
+ * hashed from its parent block's hash, its tokens and extra metadata, so equal prefixes give
+ * equal chains; "Beyond the Two Techniques": a tenant salt mixed into the hash keeps tenants'
+ * caches apart).  The cache points at allocator blocks and holds one reference per block it
+ * registers.  Host only; not thread-safe. */
+typedef struct pkv_pcache pkv_pcache;
+
+/* The hash of one block: parent_hash (0 for the first block), salt, n tokens, extra. */
+uint64_t pkv_block_hash(uint64_t parent_hash, uint64_t salt, const int32_t* tokens, int n,
+                        uint64_t extra);
+pkv_pcache* pkv_pcache_create(pkv_alloc* a);
+void pkv_pcache_destroy(pkv_pcache* pc); /* drops the cache's references */
+/* Longest chain of cached full blocks that spells the first tokens of `tokens` under `salt`;
+ * writes their ids to blocks_out (at most max_blocks) and returns how many (matched tokens =
+ * count * B), -1 on bad arguments.  Entries compare their tokens, so a hash collision never
+ * matches.  Marks the matched entries most recently used. */
+int pkv_pcache_match(pkv_pcache* pc, const int32_t* tokens, int64_t n, uint64_t salt,
+                     int32_t* blocks_out, int max_blocks);
+/* Registers the full blocks of seq_id's first n tokens (`tokens` are those tokens) under
+ * `salt`; returns the number of newly cached blocks, -1 on bad arguments / unknown seq. */
+int pkv_pcache_insert(pkv_pcache* pc, int64_t seq_id, const int32_t* tokens, int64_t n,
+                      uint64_t salt);
+/* Drops least recently used entries whose block only the cache still holds until the
+ * allocator has at least min_free free blocks (or nothing is left to drop); returns the
+ * number dropped. */
+int64_t pkv_pcache_evict(pkv_pcache* pc, int64_t min_free);
+int64_t pkv_pcache_size(const pkv_pcache* pc);
+
+/* ---------------------------------------------------------------- prefix reuse: radix tree
+ * Radix tree (compressed trie) of token sequences over the allocator's blocks (aitalk.it,
+ * "RadixAttention: A Tree That Does Not Forget"; khotyn.com, "RadixAttention"; aifetchly
+ * SGLang guide, "Radix Tree Topology", "Dynamic Node Splitting and Branch Insertion", "LRU
+ * Leaf Eviction").  Edges carry token runs, nodes the blocks holding those positions (one
+ * reference each).  Host only; not thread-safe. */
+typedef struct pkv_radix pkv_radix;
+
+pkv_radix* pkv_radix_create(pkv_alloc* a);
+void pkv_radix_destroy(pkv_radix* t); /* drops the tree's references */
+/* Longest common prefix of `tokens` with the tree, in tokens (token granularity); writes the
+ * blocks of positions [0, m) to blocks_out[0 .. ceil(m / B)) (entries at index >= max_blocks are
+ * skipped).  Pass them to pkv_alloc_add_seq_shared; a partial last block is copied on the
+ * sequence's first append.  Marks the path most recently used.  -1 on bad arguments. */
+int64_t pkv_radix_match(pkv_radix* t, const int32_t* tokens, int64_t n, int32_t* blocks_out,
+                        int max_blocks);
+/* Inserts seq_id's first n tokens (`tokens`), splitting an edge where they diverge from the
+ * tree; new positions reference seq_id's blocks.  PKV_ERR_NOT_FOUND for an unknown seq or one
+ * holding fewer than n tokens. */
+pkv_status pkv_radix_insert(pkv_radix* t, int64_t seq_id, const int32_t* tokens, int64_t n);
+/* delta = +1 / -1 on the lock count of every node on the path of an inserted token sequence
+ * (an active request uses it); locked nodes are never evicted.  PKV_ERR_NOT_FOUND if the path
+ * does not end on a node boundary (insert the sequence first). */
+pkv_status pkv_radix_lock(pkv_radix* t, const int32_t* tokens, int64_t n, int delta);
+/* Evicts least recently used unlocked leaves until the allocator has at least min_free free
+ * blocks (e.g. 10 % of the pool) or no unlocked leaf is left; a parent left with one child is
+ * merged with it.  Returns the number of leaves evicted. */
+int64_t pkv_radix_evict(pkv_radix* t, int64_t min_free);
+int64_t pkv_radix_num_nodes(const pkv_radix* t);
+int64_t pkv_radix_cached_tokens(const pkv_radix* t);
 
 #ifdef __cplusplus
 }

@@ -95,6 +95,39 @@ def _load():
     lib.pkv_alloc_seq_len.argtypes = [vp, i64]
     lib.pkv_alloc_seq_num_blocks.restype = i64
     lib.pkv_alloc_seq_num_blocks.argtypes = [vp, i64]
+    lib.pkv_alloc_add_seq_shared.restype = ctypes.c_int
+    lib.pkv_alloc_add_seq_shared.argtypes = [vp, i64, P(i32), ctypes.c_int, i64]
+    u64 = ctypes.c_uint64
+    lib.pkv_block_hash.restype = u64
+    lib.pkv_block_hash.argtypes = [u64, u64, P(i32), ctypes.c_int, u64]
+    lib.pkv_pcache_create.restype = vp
+    lib.pkv_pcache_create.argtypes = [vp]
+    lib.pkv_pcache_destroy.restype = None
+    lib.pkv_pcache_destroy.argtypes = [vp]
+    lib.pkv_pcache_match.restype = ctypes.c_int
+    lib.pkv_pcache_match.argtypes = [vp, P(i32), i64, u64, P(i32), ctypes.c_int]
+    lib.pkv_pcache_insert.restype = ctypes.c_int
+    lib.pkv_pcache_insert.argtypes = [vp, i64, P(i32), i64, u64]
+    lib.pkv_pcache_evict.restype = i64
+    lib.pkv_pcache_evict.argtypes = [vp, i64]
+    lib.pkv_pcache_size.restype = i64
+    lib.pkv_pcache_size.argtypes = [vp]
+    lib.pkv_radix_create.restype = vp
+    lib.pkv_radix_create.argtypes = [vp]
+    lib.pkv_radix_destroy.restype = None
+    lib.pkv_radix_destroy.argtypes = [vp]
+    lib.pkv_radix_match.restype = i64
+    lib.pkv_radix_match.argtypes = [vp, P(i32), i64, P(i32), ctypes.c_int]
+    lib.pkv_radix_insert.restype = ctypes.c_int
+    lib.pkv_radix_insert.argtypes = [vp, i64, P(i32), i64]
+    lib.pkv_radix_lock.restype = ctypes.c_int
+    lib.pkv_radix_lock.argtypes = [vp, P(i32), i64, ctypes.c_int]
+    lib.pkv_radix_evict.restype = i64
+    lib.pkv_radix_evict.argtypes = [vp, i64]
+    lib.pkv_radix_num_nodes.restype = i64
+    lib.pkv_radix_num_nodes.argtypes = [vp]
+    lib.pkv_radix_cached_tokens.restype = i64
+    lib.pkv_radix_cached_tokens.argtypes = [vp]
     _lib = lib
     return lib
 
@@ -262,6 +295,12 @@ class BlockAllocator:
     def add_seq(self, seq_id: int, num_tokens: int) -> None:
         _check("pkv_alloc_add_seq", self._lib.pkv_alloc_add_seq(self._h, seq_id, num_tokens))
 
+    def add_seq_shared(self, seq_id: int, shared_blocks, num_tokens: int) -> None:
+        """New sequence whose first blocks are existing (shared) blocks."""
+        arr = (ctypes.c_int32 * max(len(shared_blocks), 1))(*shared_blocks)
+        _check("pkv_alloc_add_seq_shared", self._lib.pkv_alloc_add_seq_shared(
+            self._h, seq_id, arr, len(shared_blocks), num_tokens))
+
     def fork(self, parent: int, child: int) -> None:
         _check("pkv_alloc_fork", self._lib.pkv_alloc_fork(self._h, parent, child))
 
@@ -297,3 +336,91 @@ class BlockAllocator:
 
     def seq_num_blocks(self, seq_id: int) -> int:
         return int(self._lib.pkv_alloc_seq_num_blocks(self._h, seq_id))
+
+
+def _i32(values):
+    values = list(values)
+    return (ctypes.c_int32 * max(len(values), 1))(*values), len(values)
+
+
+def block_hash(parent_hash: int, salt: int, tokens, extra: int = 0) -> int:
+    arr, n = _i32(tokens)
+    return int(_load().pkv_block_hash(parent_hash, salt, arr, n, extra))
+
+
+class PrefixCache:
+    """Chained block-hash prefix cache (libpkv pkv_pcache) over a BlockAllocator."""
+
+    def __init__(self, alloc: BlockAllocator):
+        self._lib = _load()
+        self.alloc = alloc
+        self._h = self._lib.pkv_pcache_create(alloc._h)
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_pcache_destroy(self._h)
+            self._h = None
+
+    def match(self, tokens, salt: int = 0) -> list:
+        arr, n = _i32(tokens)
+        out = (ctypes.c_int32 * max(n // self.alloc.block_size, 1))()
+        k = self._lib.pkv_pcache_match(self._h, arr, n, salt, out, n // self.alloc.block_size)
+        if k < 0:
+            raise ValueError("pkv_pcache_match: bad arguments")
+        return list(out[:k])
+
+    def insert(self, seq_id: int, tokens, salt: int = 0) -> int:
+        arr, n = _i32(tokens)
+        k = self._lib.pkv_pcache_insert(self._h, seq_id, arr, n, salt)
+        if k < 0:
+            raise ValueError("pkv_pcache_insert: unknown sequence or too few tokens")
+        return k
+
+    def evict(self, min_free: int) -> int:
+        return int(self._lib.pkv_pcache_evict(self._h, min_free))
+
+    def __len__(self):
+        return int(self._lib.pkv_pcache_size(self._h))
+
+
+class RadixTree:
+    """Radix tree of token sequences (libpkv pkv_radix) over a BlockAllocator."""
+
+    def __init__(self, alloc: BlockAllocator):
+        self._lib = _load()
+        self.alloc = alloc
+        self._h = self._lib.pkv_radix_create(alloc._h)
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_radix_destroy(self._h)
+            self._h = None
+
+    def match(self, tokens):
+        """(matched token count, blocks of the matched positions)."""
+        arr, n = _i32(tokens)
+        nb = -(-n // self.alloc.block_size)
+        out = (ctypes.c_int32 * max(nb, 1))()
+        m = int(self._lib.pkv_radix_match(self._h, arr, n, out, nb))
+        if m < 0:
+            raise ValueError("pkv_radix_match: bad arguments")
+        return m, list(out[:-(-m // self.alloc.block_size)])
+
+    def insert(self, seq_id: int, tokens) -> None:
+        arr, n = _i32(tokens)
+        _check("pkv_radix_insert", self._lib.pkv_radix_insert(self._h, seq_id, arr, n))
+
+    def lock(self, tokens, delta: int = 1) -> None:
+        arr, n = _i32(tokens)
+        _check("pkv_radix_lock", self._lib.pkv_radix_lock(self._h, arr, n, delta))
+
+    def evict(self, min_free: int) -> int:
+        return int(self._lib.pkv_radix_evict(self._h, min_free))
+
+    @property
+    def num_nodes(self) -> int:
+        return int(self._lib.pkv_radix_num_nodes(self._h))
+
+    @property
+    def cached_tokens(self) -> int:
+        return int(self._lib.pkv_radix_cached_tokens(self._h))

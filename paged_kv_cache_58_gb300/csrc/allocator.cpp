@@ -9,34 +9,14 @@
 // count reaches zero.  The khotyn.com page ("PagedAttention") adds the bound this
 // gives: at most one partially filled block per sequence.
 #include <algorithm>
-#include <new>
 #include <cstdint>
+#include <new>
 #include <unordered_map>
 #include <vector>
 
 #include "../../include/pkv.h"
 
-struct pkv_alloc {
-    struct Seq {
-        std::vector<int32_t> blocks;
-        int64_t num_tokens = 0;
-    };
-    int64_t num_blocks = 0;
-    int block_size = 16;
-    std::vector<int32_t> free_list;  // stack: back() is handed out next
-    std::vector<int32_t> refcount;
-    std::unordered_map<int64_t, Seq> seqs;
-
-    int32_t take() {
-        const int32_t b = free_list.back();
-        free_list.pop_back();
-        refcount[b] = 1;
-        return b;
-    }
-    void release(int32_t b) {
-        if (--refcount[b] == 0) free_list.push_back(b);
-    }
-};
+#include "alloc_internal.h"
 
 namespace {
 
@@ -86,6 +66,30 @@ pkv_status pkv_alloc_add_seq(pkv_alloc* a, int64_t seq_id, int64_t num_tokens) {
     s.num_tokens = num_tokens;
     s.blocks.reserve(static_cast<size_t>(need));
     for (int64_t i = 0; i < need; ++i) s.blocks.push_back(a->take());
+    a->seqs.emplace(seq_id, std::move(s));
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_add_seq_shared(pkv_alloc* a, int64_t seq_id, const int32_t* shared_blocks,
+                                    int num_shared, int64_t num_tokens) {
+    if (!a || num_shared < 0 || num_tokens < 0 || (num_shared > 0 && !shared_blocks))
+        return PKV_ERR_INVALID;
+    if (a->seqs.count(seq_id)) return PKV_ERR_NOT_FOUND;
+    const int64_t need = blocks_for(num_tokens, a->block_size);
+    if (num_shared > need) return PKV_ERR_INVALID;
+    for (int i = 0; i < num_shared; ++i) {
+        const int32_t b = shared_blocks[i];
+        if (b < 0 || b >= a->num_blocks || a->refcount[b] <= 0) return PKV_ERR_INVALID;
+    }
+    if (need - num_shared > static_cast<int64_t>(a->free_list.size())) return PKV_ERR_NOMEM;
+    pkv_alloc::Seq s;
+    s.num_tokens = num_tokens;
+    s.blocks.reserve(static_cast<size_t>(need));
+    for (int i = 0; i < num_shared; ++i) {
+        ++a->refcount[shared_blocks[i]];
+        s.blocks.push_back(shared_blocks[i]);
+    }
+    for (int64_t i = num_shared; i < need; ++i) s.blocks.push_back(a->take());
     a->seqs.emplace(seq_id, std::move(s));
     return PKV_OK;
 }
