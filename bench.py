@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--workload", choices=DECODE_WORKLOADS, default="8b",
                    help="decode workload of the step (default: the Llama-3-8B-shaped batch)")
+    p.add_argument("--cascade", action="store_true",
+                   help="shared workload: decode with the shared-prefix cascade")
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--prefill-steps", type=int, default=20)
     p.add_argument("--min-warm-seconds", type=float, default=1.0,
@@ -310,12 +312,28 @@ def main():
     max_parts = math.ceil(math.ceil(max_ctx / 16) / pb)
     launches_per_step = 2 + (1 if max_parts > 1 else 0)
 
+    cascade = args.cascade and case.wl.shared_prefix > 0
+    if cascade:
+        plen = case.wl.shared_prefix
+        prefix_blocks = case.block_tables[0, :plen // 16].contiguous()
+        wsz = pkv.cascade_workspace_bytes(S, Hq, D, plen, max_ctx)
+        workspace = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
+        launches_per_step = 4
+
+    def decode(q, bt, cl):
+        if cascade:
+            pkv.paged_decode_cascade(q, case.k_pool, case.v_pool, prefix_blocks, plen, bt, cl,
+                                     case.scale, max_context=max_ctx, out=out,
+                                     workspace=workspace, stream=stream)
+        else:
+            pkv.paged_decode(q, case.k_pool, case.v_pool, bt, cl, case.scale,
+                             max_context=max_ctx, out=out, partition_blocks=0,
+                             workspace=workspace, stream=stream)
+
     def step():
         pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new,
                       stream=stream)
-        pkv.paged_decode(case.q, case.k_pool, case.v_pool, case.block_tables,
-                         case.context_lens, case.scale, max_context=max_ctx, out=out,
-                         partition_blocks=0, workspace=workspace, stream=stream)
+        decode(case.q, case.block_tables, case.context_lens)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -342,9 +360,7 @@ def main():
         pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new,
                       stream=stream)
         ev[i][0].record(stream)
-        pkv.paged_decode(case.q, case.k_pool, case.v_pool, case.block_tables,
-                         case.context_lens, case.scale, max_context=max_ctx, out=out,
-                         partition_blocks=0, workspace=workspace, stream=stream)
+        decode(case.q, case.block_tables, case.context_lens)
         ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -380,9 +396,7 @@ def main():
                 devb[n].copy_(t, non_blocking=True)
             pkv.kv_append(case.k_pool, case.v_pool, devb["slot_mapping"], devb["k_new"],
                           devb["v_new"], stream=stream)
-            pkv.paged_decode(devb["q"], case.k_pool, case.v_pool, devb["block_tables"],
-                             devb["context_lens"], case.scale, max_context=max_ctx, out=out,
-                             workspace=workspace, stream=stream)
+            decode(devb["q"], devb["block_tables"], devb["context_lens"])
             out_h.copy_(out, non_blocking=True)
             stream.synchronize()
 
@@ -434,8 +448,10 @@ def main():
                    "l2": ("inputs larger than L2 (K/V read per step > 129 MB L2)"
                           if decode_bytes > 2 * 129e6 else
                           "K/V per step smaller than L2: warm-cache figure"),
-                   "parallelism": f"replicas x{ws}"},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode (decode_tc split-KV + combine)",
+                   "parallelism": f"replicas x{ws}", "cascade": cascade},
+        "roofline": {"bound": "hbm",
+                     "kernel": ("paged_decode_cascade (prefix pass + suffix split-KV + combine)"
+                                if cascade else "paged_decode (decode_tc split-KV + combine)"),
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,

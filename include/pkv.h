@@ -149,6 +149,31 @@ pkv_status pkv_paged_decode_noalloc(const pkv_pool_desc* pool, void* out, const 
                                     int num_q_heads, float scale, int partition_blocks,
                                     void* stream);
 
+/* ---------------------------------------------------------------- cascade decode
+ * Decode of sequences that all begin with the same prefix_len tokens held in the same physical
+ * blocks (a prompt shared through the block tables: Triptych page, "Sharing is a pointer
+ * change"; aitalk.it, "RadixAttention").  The result equals pkv_paged_decode's; the work is
+ * arranged so that the shared blocks are read once: (1) every sequence's query heads attend
+ * the prefix blocks as one tensor-core pass (the prefill kernel with no causal mask), (2) each
+ * sequence's private suffix (tokens from prefix_len on) is decoded with split-KV partitions,
+ * (3) the log-sum-exp combine merges the prefix partial with the suffix partials.
+ *   prefix_blocks  device int32 [prefix_len / block_size]: the shared blocks; every
+ *                  sequence's block_tables row must start with them.
+ *   prefix_len     > 0, a multiple of block_size; context_lens[s] >= prefix_len.
+ *   max_context    host upper bound of context_lens (>= prefix_len).
+ *   workspace      >= pkv_paged_decode_cascade_workspace_bytes(...) bytes, 16-byte aligned.
+ * Other arguments as pkv_paged_decode.  Requires PKV_BF16 and head_dim 128. */
+size_t pkv_paged_decode_cascade_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                                int prefix_len, int max_context, int block_size,
+                                                int partition_blocks);
+pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const void* q,
+                                    const void* k_pool, const void* v_pool,
+                                    const int32_t* prefix_blocks, int prefix_len,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int max_context, int num_seqs,
+                                    int num_q_heads, float scale, int partition_blocks,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- paged_prefill
  * Causal prefill of new tokens over a cached prefix ("computes only the unseen
  * suffix" while reusing the cached prefix's K/V: aitalk.it, "RadixAttention: A Tree

@@ -97,6 +97,12 @@ def _load():
     lib.pkv_alloc_seq_num_blocks.argtypes = [vp, i64]
     lib.pkv_alloc_add_seq_shared.restype = ctypes.c_int
     lib.pkv_alloc_add_seq_shared.argtypes = [vp, i64, P(i32), ctypes.c_int, i64]
+    lib.pkv_paged_decode_cascade_workspace_bytes.restype = sz
+    lib.pkv_paged_decode_cascade_workspace_bytes.argtypes = [ctypes.c_int] * 7
+    lib.pkv_paged_decode_cascade.restype = ctypes.c_int
+    lib.pkv_paged_decode_cascade.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, ctypes.c_int, vp,
+                                             ctypes.c_int, vp, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, f32, ctypes.c_int, vp, sz, vp]
     u64 = ctypes.c_uint64
     lib.pkv_block_hash.restype = u64
     lib.pkv_block_hash.argtypes = [u64, u64, P(i32), ctypes.c_int, u64]
@@ -228,6 +234,35 @@ def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *, max_co
                                   int(max_context), S, Hq, float(scale), int(partition_blocks),
                                   wptr, wbytes, _stream(stream))
     _check("pkv_paged_decode", st)
+    return out
+
+
+def cascade_workspace_bytes(num_seqs, num_q_heads, head_dim, prefix_len, max_context,
+                            partition_blocks=0):
+    return int(_load().pkv_paged_decode_cascade_workspace_bytes(
+        num_seqs, num_q_heads, head_dim, prefix_len, max_context, BLOCK_SIZE, partition_blocks))
+
+
+def paged_decode_cascade(q, k_pool, v_pool, prefix_blocks, prefix_len, block_tables,
+                         context_lens, scale, *, max_context, out=None, partition_blocks=0,
+                         workspace=None, stream=None):
+    """Decode of sequences sharing their first `prefix_len` tokens in `prefix_blocks`
+    (int32 [prefix_len / 16] CUDA tensor); same result as paged_decode."""
+    d = pool_desc(k_pool)
+    S, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    need = cascade_workspace_bytes(S, Hq, D, prefix_len, max_context, partition_blocks)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = _load().pkv_paged_decode_cascade(
+        ctypes.byref(d), _dev(out, "out", q.dtype), _dev(q, "q", k_pool.dtype),
+        _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
+        _dev(prefix_blocks, "prefix_blocks", torch.int32), int(prefix_len),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), int(max_context), S, Hq, float(scale),
+        int(partition_blocks), workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check("pkv_paged_decode_cascade", st)
     return out
 
 

@@ -49,8 +49,14 @@ struct DecodeArgs {
     int num_q_heads;
     int num_kv_heads;
     int partition_blocks;
-    int max_parts;
+    int max_parts;     // partitions of the decoded block range per sequence
     float scale_log2;  // softmax scale * log2(e)
+    // Cascade decode: blocks [0, block_offset) of every sequence were handled by a
+    // separate shared-prefix pass whose partial sits at partition 0; the split kernel
+    // covers blocks [block_offset, nblk) into partitions extra_parts.. and the combine
+    // merges extra_parts + max_parts partials per row.
+    int block_offset;
+    int extra_parts;
 };
 
 // CUDA-core decode (fp32 and bf16 pools): split kernel + combine.
@@ -97,6 +103,17 @@ struct PrefillArgs {
     int num_q_heads;
     int num_kv_heads;
     float scale_log2;
+    // Cascade mode (shared-prefix decode): one "request" whose cached_lens[0] keys are
+    // the shared prefix and whose new_lens[0] query rows are the sequences (one token
+    // each); every row attends all prefix keys (no causal mask) and the result goes to
+    // the split-KV partials (partition 0 of max_parts_total) instead of `out`.
+    int cascade;
+    int cascade_keys;   // cascade: prefix length (keys); rows come from cascade_rows
+    int cascade_rows;   // cascade: number of sequences (query rows per head)
+    int max_parts_total;
+    float* o_part;
+    float* m_part;
+    float* l_part;
 };
 
 cudaError_t launch_paged_prefill(const PrefillArgs& a, int group, cudaStream_t stream);

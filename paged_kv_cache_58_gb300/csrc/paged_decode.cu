@@ -150,12 +150,13 @@ decode_split_kernel(const DecodeArgs a) {
     const int c = lane & 15;    // D slice
 
     int L = a.context_lens[seq];
-    if (L > a.max_blocks_per_seq * kBlock || L > a.max_parts * a.partition_blocks * kBlock) {
+    const int span_end = a.block_offset + a.max_parts * a.partition_blocks;  // blocks covered
+    if (L > a.max_blocks_per_seq * kBlock || L > span_end * kBlock) {
         if (part == 0 && threadIdx.x == 0) raise_status(a.status, PKV_ERR_OOB);
-        L = min(a.max_blocks_per_seq, a.max_parts * a.partition_blocks) * kBlock;
+        L = min(a.max_blocks_per_seq, span_end) * kBlock;
     }
     const int nblk = (L + kBlock - 1) / kBlock;
-    const int b0 = part * a.partition_blocks;
+    const int b0 = a.block_offset + part * a.partition_blocks;
     if (L <= 0 || b0 >= nblk) return;  // uniform over the CTA, before any barrier
     const int b1 = min(nblk, b0 + a.partition_blocks);
     const int my_first = b0 + warp;
@@ -334,7 +335,7 @@ decode_split_kernel(const DecodeArgs a) {
     }
     __syncthreads();
 
-    const int nparts = a.max_parts;
+    const int nparts = a.max_parts + a.extra_parts;   // partial slots per row
     for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
         const int g = idx / D;
         const int d = idx % D;
@@ -353,7 +354,7 @@ decode_split_kernel(const DecodeArgs a) {
         if (nparts == 1) {
             store_elem<T>(static_cast<T*>(a.out) + row * D + d, o / l);
         } else {
-            const size_t pr = row * nparts + part;
+            const size_t pr = row * nparts + a.extra_parts + part;
             a.o_part[pr * D + d] = o / l;
             if (d == 0) {
                 a.m_part[pr] = M;
@@ -383,17 +384,20 @@ decode_combine_kernel(const DecodeArgs a) {
     const int seq = static_cast<int>(row / a.num_q_heads);
     const int L = min(a.context_lens[seq], a.max_blocks_per_seq * kBlock);
     const int nblk = (L + kBlock - 1) / kBlock;
-    const int np = min(a.max_parts, (nblk + a.partition_blocks - 1) / a.partition_blocks);
+    const int total = a.max_parts + a.extra_parts;   // partial slots per row
+    const int np = a.extra_parts +
+                   min(a.max_parts, max(0, (nblk - a.block_offset + a.partition_blocks - 1) /
+                                               a.partition_blocks));
     if (np <= 0) return;
-    const float* mp = a.m_part + row * a.max_parts;
-    const float* lp = a.l_part + row * a.max_parts;
+    const float* mp = a.m_part + row * total;
+    const float* lp = a.l_part + row * total;
 
     float M = -INFINITY;
     for (int p = lane; p < np; p += 32) M = fmaxf(M, mp[p]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
-    const float* op = a.o_part + row * a.max_parts * D + lane * EL;
+    const float* op = a.o_part + row * total * D + lane * EL;
     float acc[EL];
 #pragma unroll
     for (int e = 0; e < EL; ++e) acc[e] = 0.f;
@@ -443,9 +447,12 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SM::kTotal);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
-    e = launch_pdl(kern, grid, dim3(kThreads), SM::kTotal, stream, a);
-    if (e != cudaSuccess || a.max_parts == 1) return e;
+    if (a.max_parts > 0) {   // zero when a cascade decode has no private suffix at all
+        dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
+        e = launch_pdl(kern, grid, dim3(kThreads), SM::kTotal, stream, a);
+        if (e != cudaSuccess) return e;
+    }
+    if (a.extra_parts == 0 && a.max_parts == 1) return e;  // output written directly
     return launch_decode_combine(a, sizeof(T) == 2 ? PKV_BF16 : PKV_F32, D, stream);
 }
 

@@ -101,12 +101,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int lane = threadIdx.x & 31;
 
     int L = a.context_lens[seq];
-    if (L > a.max_blocks_per_seq * kBlk || L > a.max_parts * a.partition_blocks * kBlk) {
+    const int span_end = a.block_offset + a.max_parts * a.partition_blocks;  // blocks covered
+    if (L > a.max_blocks_per_seq * kBlk || L > span_end * kBlk) {
         if (part == 0 && threadIdx.x == 0) raise_status(a.status, PKV_ERR_OOB);
-        L = min(a.max_blocks_per_seq, a.max_parts * a.partition_blocks) * kBlk;
+        L = min(a.max_blocks_per_seq, span_end) * kBlk;
     }
     const int nblk = (L + kBlk - 1) / kBlk;
-    const int b0 = part * a.partition_blocks;
+    const int b0 = a.block_offset + part * a.partition_blocks;
     if (L <= 0 || b0 >= nblk) return;  // uniform over the CTA, before any barrier
     const int b1 = min(nblk, b0 + a.partition_blocks);
     const int my_first = b0 + warp;
@@ -320,7 +321,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
     __syncthreads();
 
-    const int nparts = a.max_parts;
+    const int nparts = a.max_parts + a.extra_parts;   // partial slots per row
     for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
         const int g = idx / D;
         const int d = idx % D;
@@ -339,7 +340,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             static_cast<uint16_t*>(a.out)[row * D + d] =
                 static_cast<uint16_t>(pack_bf16x2(o / l, 0.f) & 0xffffu);
         } else {
-            const size_t pr = row * nparts + part;
+            const size_t pr = row * nparts + a.extra_parts + part;
             a.o_part[pr * D + d] = o / l;
             if (d == 0) {
                 a.m_part[pr] = M;
@@ -360,9 +361,12 @@ cudaError_t launch_tc(const DecodeArgs& a, cudaStream_t stream) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
-    e = launch_pdl(kern, grid, dim3(kThreads), SM::kTotal, stream, mk, mv, a);
-    if (e != cudaSuccess || a.max_parts == 1) return e;
+    if (a.max_parts > 0) {   // zero when a cascade decode has no private suffix at all
+        dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
+        e = launch_pdl(kern, grid, dim3(kThreads), SM::kTotal, stream, mk, mv, a);
+        if (e != cudaSuccess) return e;
+    }
+    if (a.extra_parts == 0 && a.max_parts == 1) return e;  // output written directly
     return launch_decode_combine(a, PKV_BF16, D, stream);
 }
 

@@ -129,19 +129,21 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const int n = a.new_lens[r];
-    const int c = a.cached_lens[r];
+    const bool cascade = a.cascade != 0;    // rows = sequences over the c shared keys
+    const int n = cascade ? a.cascade_rows : a.new_lens[r];
+    const int c = cascade ? a.cascade_keys : a.cached_lens[r];
     const int t0 = qt * TOK;
     if (t0 >= n) return;  // uniform over the CTA, before any barrier or TMEM use
-    const int L = c + n;
-    if (c < 0 || L > a.max_blocks_per_seq * kBlk) {
+    const int L = cascade ? c : c + n;       // keys in the pool for this request
+    if (c < 0 || L <= 0 || L > a.max_blocks_per_seq * kBlk) {
         if (threadIdx.x == 0) raise_status(a.status, PKV_ERR_OOB);
         return;
     }
     const int i_last = min(t0 + TOK, n) - 1;
-    const int max_lim = c + i_last;          // last key any row of this tile sees
+    const int max_lim = cascade ? c - 1 : c + i_last;   // last key any row of this tile sees
     const int ntiles = max_lim / kKeys + 1;
-    const int qrow0 = a.q_offsets[r] + t0;   // first token row of the tile in q / out
+    const int qoff = cascade ? 0 : a.q_offsets[r];
+    const int qrow0 = qoff + t0;             // first token row of the tile in q / out
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
@@ -292,7 +294,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int tok = t0 + row / G;
         const int head = kvh * G + row % G;
         const bool row_valid = tok < n;
-        const int lim = row_valid ? c + tok : c + n - 1;   // last key this row sees
+        const int lim = cascade ? c - 1 : (row_valid ? c + tok : c + n - 1);  // last key seen
         const float sl2 = a.scale_log2;
         float m_used = -INFINITY;
         float l = 0.f;
@@ -407,15 +409,26 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                                 ((ntiles - 1) / kBufs) & 1, lane)) {
             tc_fence_after();
             const float inv_l = 1.f / l;
-            uint16_t* orow = static_cast<uint16_t*>(a.out) +
-                             (static_cast<size_t>(a.q_offsets[r] + tok) * a.num_q_heads + head) *
-                                 kHead;
+            const size_t orow_idx = static_cast<size_t>(qoff + tok) * a.num_q_heads + head;
+            uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * kHead;
+            const size_t prow = orow_idx * a.max_parts_total;   // cascade: partition 0
+            if (cascade && row_valid) {
+                a.m_part[prow] = m_used;   // log2 domain, as the decode partials
+                a.l_part[prow] = l;
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float o[32];
                 tmem_ld32(tmem + lane_addr + kTmemO + q * 32, o);
                 tmem_wait_ld();
-                if (row_valid) {
+                if (cascade && row_valid) {
+                    float* dst = a.o_part + prow * kHead + q * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(dst + e) =
+                            make_float4(o[e] * inv_l, o[e + 1] * inv_l, o[e + 2] * inv_l,
+                                        o[e + 3] * inv_l);
+                } else if (row_valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         uint4 w;

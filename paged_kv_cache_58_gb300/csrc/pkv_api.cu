@@ -258,6 +258,118 @@ pkv_status pkv_paged_decode_noalloc(const pkv_pool_desc* pool, void* out, const 
                             partition_blocks, scratch, need, stream);
 }
 
+size_t pkv_paged_decode_cascade_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                                int prefix_len, int max_context, int block_size,
+                                                int partition_blocks) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || prefix_len <= 0 ||
+        max_context < prefix_len || block_size != kBlockSize || partition_blocks < 0)
+        return 0;
+    const int suffix = max_context - prefix_len;
+    const int pb = partition_blocks ? partition_blocks
+                                    : (suffix > 0 ? auto_partition(num_seqs, suffix) : 1);
+    const int parts = suffix > 0 ? ceil_div(ceil_div(suffix, kBlockSize), pb) : 0;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * (parts + 1);
+    const size_t ml = (rows * sizeof(float) + 15) / 16 * 16;
+    return rows * head_dim * sizeof(float) + 2 * ml;
+}
+
+pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const void* q,
+                                    const void* k_pool, const void* v_pool,
+                                    const int32_t* prefix_blocks, int prefix_len,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int max_context, int num_seqs,
+                                    int num_q_heads, float scale, int partition_blocks,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+    pkv_status st = check_pool(pool);
+    if (st != PKV_OK) return st;
+    if (num_seqs < 0 || num_q_heads <= 0 || partition_blocks < 0 || !(scale > 0.f))
+        return PKV_ERR_INVALID;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !prefix_blocks || !block_tables || !context_lens)
+        return PKV_ERR_INVALID;
+    if (prefix_len <= 0 || prefix_len % kBlockSize != 0 || max_context < prefix_len ||
+        max_blocks_per_seq <= 0 ||
+        static_cast<int64_t>(max_context) > static_cast<int64_t>(max_blocks_per_seq) * kBlockSize)
+        return PKV_ERR_INVALID;
+    if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID;
+    const int group = num_q_heads / pool->num_kv_heads;
+    if (pool->dtype != PKV_BF16 || pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PKV_ERR_INVALID;
+    const int suffix = max_context - prefix_len;
+    const int pb = partition_blocks ? partition_blocks
+                                    : (suffix > 0 ? auto_partition(num_seqs, suffix) : 1);
+    const int parts = suffix > 0 ? ceil_div(ceil_div(suffix, kBlockSize), pb) : 0;
+    if (parts + 1 > pkv::kMaxParts) return PKV_ERR_UNSUPPORTED;
+    const size_t need = pkv_paged_decode_cascade_workspace_bytes(
+        num_seqs, num_q_heads, pool->head_dim, prefix_len, max_context, kBlockSize,
+        partition_blocks);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_NOMEM;
+    int* status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * (parts + 1);
+    const size_t ml = (rows * sizeof(float) + 15) / 16 * 16;
+    char* w = static_cast<char*>(workspace);
+    float* o_part = reinterpret_cast<float*>(w);
+    float* m_part = reinterpret_cast<float*>(w + rows * pool->head_dim * sizeof(float));
+    float* l_part = reinterpret_cast<float*>(w + rows * pool->head_dim * sizeof(float) + ml);
+    const float sl2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+
+    // 1. every sequence's query heads against the shared prefix, on the tensor cores
+    pkv::PrefillArgs pa{};
+    pa.q = q;
+    pa.k_pool = k_pool;
+    pa.v_pool = v_pool;
+    pa.block_tables = prefix_blocks;
+    pa.status = status;
+    pa.num_blocks = pool->num_blocks;
+    pa.max_blocks_per_seq = prefix_len / kBlockSize;
+    pa.num_reqs = 1;
+    pa.total_new = num_seqs;
+    pa.max_new = num_seqs;
+    pa.num_q_heads = num_q_heads;
+    pa.num_kv_heads = pool->num_kv_heads;
+    pa.scale_log2 = sl2;
+    pa.cascade = 1;
+    pa.cascade_keys = prefix_len;
+    pa.cascade_rows = num_seqs;
+    pa.max_parts_total = parts + 1;
+    pa.o_part = o_part;
+    pa.m_part = m_part;
+    pa.l_part = l_part;
+    cudaError_t e = pkv::launch_paged_prefill(pa, group, st_);
+    if (e != cudaSuccess) return e == cudaErrorNotSupported ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
+
+    // 2. private suffixes (blocks from prefix_len / B on) + 3. log-sum-exp merge
+    pkv::DecodeArgs a{};
+    a.out = out;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.status = status;
+    a.num_blocks = pool->num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = pool->num_kv_heads;
+    a.partition_blocks = pb;
+    a.max_parts = parts;
+    a.scale_log2 = sl2;
+    a.o_part = o_part;
+    a.m_part = m_part;
+    a.l_part = l_part;
+    a.block_offset = prefix_len / kBlockSize;
+    a.extra_parts = 1;
+    if (decode_use_simt())
+        return from_cuda(pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_));
+    return from_cuda(pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_));
+}
+
 pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q,
                              const void* k_pool, const void* v_pool,
                              const int32_t* block_tables, int max_blocks_per_seq,
