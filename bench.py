@@ -186,6 +186,14 @@ def kernel_traffic(kernel_src: str, summary: str):
     return None
 
 
+def aggregate(elapsed: float, units_per_rank: float, ws: int, all_reduce_max=None):
+    """Whole-job rate over `ws` independent replicas: the time is the slowest rank's
+    (max over ranks), the work the sum over ranks.  `all_reduce_max` maps a local float
+    to the max over ranks (None: one rank)."""
+    t = all_reduce_max(elapsed) if all_reduce_max else elapsed
+    return ws * units_per_rank / t, t
+
+
 def workload_bytes(case):
     """Algorithmic bytes of one step: decode reads every attended K/V row once, q,
     block-table entries and context lengths once, writes out once; kv_append reads
@@ -369,16 +377,20 @@ def main():
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
     decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
+
+    def max_over_ranks(x: float) -> float:
+        t = torch.tensor([x], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        return float(t.item())
+
+    reducer = max_over_ranks if ws > 1 else None
     assert pkv.read_device_status() == 0
 
-    ms_step = total_ms / K
     step_bytes = decode_bytes + append_bytes
-    value = ws * step_bytes / (ms_step * 1e-3) / 1e9
-    tok_s = ws * S / (ms_step * 1e-3)
+    rate, total_s = aggregate(total_ms * 1e-3, step_bytes * K, ws, reducer)
+    value = rate / 1e9
+    ms_step = total_s * 1e3 / K
+    tok_s = ws * S * K / total_s
 
     # end to end through the public API with host buffers: H2D of the step's inputs
     # from pinned memory, the two calls, D2H of the output, synchronised per step.
@@ -408,11 +420,8 @@ def main():
         for _ in range(K):
             e2e_step()
         el = time.perf_counter() - t0
-        if ws > 1:
-            t = torch.tensor([el], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            el = float(t.item())
-        e2e = {"value": ws * step_bytes * K / el / 1e9, "unit": "GB/s",
+        e2e_rate, el = aggregate(el, step_bytes * K, ws, reducer)
+        e2e = {"value": e2e_rate / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": el / K * 1e3, "tokens_per_s_per_layer": ws * S * K / el}
 
