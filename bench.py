@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--workload", choices=DECODE_WORKLOADS, default="8b",
                    help="decode workload of the step (default: the Llama-3-8B-shaped batch)")
+    p.add_argument("--partition-blocks", type=int, default=0,
+                   help="split-KV partition size in blocks (0: the library's policy)")
     p.add_argument("--cascade", action="store_true",
                    help="shared workload: decode with the shared-prefix cascade")
     p.add_argument("--no-prefill", action="store_true")
@@ -312,8 +314,8 @@ def main():
     S, Hq, D = case.q.shape
     decode_bytes, append_bytes, tokens = workload_bytes(case)
     max_ctx = case.max_context
-    pb = pkv.auto_partition(S, max_ctx)
-    wsz = pkv.decode_workspace_bytes(S, Hq, D, max_ctx)
+    pb = args.partition_blocks or pkv.auto_partition(S, Hq, max_ctx)
+    wsz = pkv.decode_workspace_bytes(S, Hq, D, max_ctx, pb)
     workspace = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
     out = torch.empty_like(case.q)
     stream = torch.cuda.current_stream(dev)
@@ -335,7 +337,7 @@ def main():
                                      workspace=workspace, stream=stream)
         else:
             pkv.paged_decode(q, case.k_pool, case.v_pool, bt, cl, case.scale,
-                             max_context=max_ctx, out=out, partition_blocks=0,
+                             max_context=max_ctx, out=out, partition_blocks=pb,
                              workspace=workspace, stream=stream)
 
     def step():

@@ -122,7 +122,8 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
 
 /* Partition size (in blocks) pkv_paged_decode uses for partition_blocks == 0; it
  * depends only on these arguments (0 for invalid ones). */
-int pkv_paged_decode_auto_partition(int num_seqs, int max_context, int block_size);
+int pkv_paged_decode_auto_partition(int num_seqs, int num_q_heads, int max_context,
+                                    int block_size);
 
 /* Same decode for callers that cannot allocate device memory: code running where
  * cudaMalloc is not allowed or not wanted (inside a caller-managed memory pool or

@@ -60,7 +60,7 @@ def _load():
     lib.pkv_paged_decode_workspace_bytes.restype = sz
     lib.pkv_paged_decode_workspace_bytes.argtypes = [ctypes.c_int] * 6
     lib.pkv_paged_decode_auto_partition.restype = ctypes.c_int
-    lib.pkv_paged_decode_auto_partition.argtypes = [ctypes.c_int] * 3
+    lib.pkv_paged_decode_auto_partition.argtypes = [ctypes.c_int] * 4
     lib.pkv_paged_decode.restype = ctypes.c_int
     lib.pkv_paged_decode.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, ctypes.c_int, vp,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, f32, ctypes.c_int,
@@ -205,8 +205,9 @@ def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context, partiti
                                                         partition_blocks))
 
 
-def auto_partition(num_seqs, max_context) -> int:
-    return int(_load().pkv_paged_decode_auto_partition(num_seqs, max_context, BLOCK_SIZE))
+def auto_partition(num_seqs, num_q_heads, max_context) -> int:
+    return int(_load().pkv_paged_decode_auto_partition(num_seqs, num_q_heads, max_context,
+                                                       BLOCK_SIZE))
 
 
 def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *, max_context,

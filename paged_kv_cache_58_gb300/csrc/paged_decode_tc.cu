@@ -32,7 +32,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kBlk = 16;
 constexpr int kBox = kBlk * 128;  // one 16-row x 64-column bf16 box
 constexpr float kLazyRescale = 8.0f;

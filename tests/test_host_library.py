@@ -188,12 +188,12 @@ def test_unknown_ids_and_small_tables(pkv):
 
 
 def test_decode_workspace_and_partition_policy(pkv):
-    # 8B-shaped batch: 64 sequences up to 4096 tokens -> 512-token partitions
-    assert pkv.auto_partition(64, 4096) == 32
+    # 8B-shaped batch: 64 sequences up to 4096 tokens -> 1024-token partitions
+    assert pkv.auto_partition(64, 32, 4096) == 64
     ws = pkv.decode_workspace_bytes(64, 32, 128, 4096)
-    assert ws == 64 * 32 * 8 * (128 + 2) * 4
+    assert ws == 64 * 32 * 4 * (128 + 2) * 4
     # 70B-shaped batch: 131072 tokens -> at most 64 partitions
-    pb = pkv.auto_partition(16, 131072)
+    pb = pkv.auto_partition(16, 64, 131072)
     assert pb == 128 and -(-8192 // pb) == 64
     # a single short sequence needs no workspace
     assert pkv.decode_workspace_bytes(1, 8, 128, 64) == 0
