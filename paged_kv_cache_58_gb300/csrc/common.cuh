@@ -60,6 +60,25 @@ PKV_DEVINL void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Predicated forms for converged warps: every lane executes the instruction and only
+// lanes with `on` perform it, so a single-lane action needs no branch (reconverging a
+// diverged warp costs hundreds of cycles on a busy scheduler).
+PKV_DEVINL void mbar_arrive_if(bool on, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "@q mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(static_cast<uint32_t>(on))
+        : "memory");
+}
+
+PKV_DEVINL void mbar_arrive_expect_tx_if(bool on, uint64_t* bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+        "@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes), "r"(static_cast<uint32_t>(on))
+        : "memory");
+}
+
 PKV_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -117,6 +136,26 @@ PKV_DEVINL void tma_load_3d(void* smem_dst, const void* tmap, int32_t x, int32_t
         : "memory");
 }
 
+PKV_DEVINL void tma_load_4d(void* smem_dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                            int32_t w, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
+PKV_DEVINL void tma_load_4d_if(bool on, void* smem_dst, const void* tmap, int32_t x, int32_t y,
+                               int32_t z, int32_t w, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %7, 0;\n\t"
+        "@q cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];\n\t}" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
+        "r"(static_cast<uint32_t>(on))
+        : "memory");
+}
+
 PKV_DEVINL void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -140,6 +179,47 @@ PKV_DEVINL float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// max(a, b, c) in one instruction (sm_100+ three-input form).
+PKV_DEVINL float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Packed pair arithmetic (sm_100+ f32x2): (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1).
+PKV_DEVINL void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                      float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+PKV_DEVINL void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Upper 16 bits of a (low half of the result) and of b (high half): two fp32 values
+// truncated to bf16 and packed, in one byte permute.
+PKV_DEVINL uint32_t pack_bf16x2_trunc(float a, float b) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(r) : "r"(__float_as_uint(a)), "r"(__float_as_uint(b)));
+    return r;
+}
+
+// One lane of the converged warp (the lowest active one) gets true.
+PKV_DEVINL bool elect_one() {
+    uint32_t p = 0;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(p));
+    return p != 0;
 }
 
 }  // namespace pkv

@@ -72,6 +72,10 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, int head_dim,
 // Tensor maps (host): a pool viewed as rows [num_blocks * Hkv * 16] x head_dim bf16,
 // box 64 columns x 16 rows, 128-byte swizzle.
 bool make_pool_map(CUtensorMap* m, const void* pool, int64_t rows, int head_dim);
+// The same pool (head_dim 128) as one box per 16-row block: dims {64 columns, 8 rows,
+// 2 column halves, rows / 8 row groups}, box {64, 8, 2, 2} = 4 KB, landing in shared
+// memory as [row group][half][8 rows][128 B] with the 128-byte swizzle.
+bool make_pool_block_map(CUtensorMap* m, const void* pool, int64_t rows);
 // q [tokens][Hq][head_dim] bf16 read as boxes of 64 columns x G heads x tok tokens.
 bool make_q_group_map(CUtensorMap* m, const void* q, int tokens, int hq, int head_dim, int G,
                       int tok);

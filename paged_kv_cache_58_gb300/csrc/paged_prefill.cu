@@ -10,35 +10,48 @@
 // One CTA computes one 128-row query tile: TOK = 128 / G consecutive new tokens x
 // the G query heads that share kv head `kvh` (rows token-major, heads inner), so
 // every K/V tile it stages serves all G heads.  Per 128-key KV tile j:
-//   S_j = Q K_j^T  tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) into TMEM
-//                  buffer j % 3
+//   S_j = Q K_j^T  tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) into the TMEM
+//                  S/P buffer of stream j % 2
 //   softmax        4 warps, one thread per row: tcgen05.ld S_j, causal mask, exp2,
-//                  row sums in fp32; P_j is split into bf16 hi + lo parts (P = hi +
-//                  lo to ~2^-17 relative) and stored back over S_j in the same TMEM
-//                  buffer (hi in its first 64 columns, lo in the next 64)
+//                  row sums in fp32; P_j is split into bf16 hi + lo parts (hi = P
+//                  truncated, lo = the remainder truncated: hi + lo within 2^-14 of P)
+//                  and stored back over S_j in the same TMEM buffer (hi in its first
+//                  64 columns, lo in the next 64)
 //   O += P_j V_j   two tcgen05.mma passes (A = P hi, then P lo, from TMEM; B = V_j
-//                  from shared memory) into a TMEM accumulator kept across tiles
-// The split keeps the probabilities at fp32-like precision: a single bf16 P is off by
-// up to 2^-9 per weight, which rows attending only a few keys do not average away.
+//                  from shared memory) into the TMEM accumulator O of stream j % 2
+// The split keeps the probabilities near fp32 precision: a single bf16 P is off by up
+// to 2^-8 per weight, which rows attending only a few keys do not average away; with
+// the split every output is within 2^-14 * max|v| of the exact weights' result.
 // The running max is updated lazily: O and l are rescaled only when a row's max
 // grows by more than 2^8, which keeps P <= 256 and leaves the result exact.
 //
-// Pipelining.  The MMA issuer runs S_{j+1} before P_j V_j; S_{j+3} reuses the
-// buffer of P_j once P_j V_j has completed (its own per-buffer barrier: MMAs with
-// different accumulators are not ordered against each other), which with three
-// buffers is normally long done.  The softmax of tile j+1 overlaps P_j V_j and waits
-// for it only when a row's max grew (O rescale).  K stages (3) are released as soon
-// as their S has run, V stages (3) after their P.V, so the gathers of the next tiles
-// are in flight while the current one is computed.  Each 16-token block of a tile
-// arrives as two TMA boxes (64 columns x 16 rows, 128-byte swizzle) per pool.
+// Two streams.  Even and odd KV tiles are two independent online-softmax passes,
+// each with its own S/P buffer, O accumulator, running max and row sum, merged by a
+// log-sum-exp step after the last tile.  Within a stream the chain S_j -> softmax ->
+// P_j V_j -> S_{j+2} (which overwrites P_j) is serial; the streams interleave, so the
+// tensor pipe works on one while the other waits for its softmax, and the softmax
+// warps always find the next S ready.  One warp issues each stream (S_j, then P_j V_j,
+// then S_{j+2} once that P.V completed: MMAs with different accumulators are not
+// ordered against each other).  K and V stages (3 each) are released when their S and
+// P.V have run, so the gathers of later tiles are in flight.  Each 16-token block of
+// a tile arrives as ONE 4-D TMA box (the block's 16 rows x 256 B viewed as 2 row
+// groups x 2 column halves x 8 rows x 128 B, 128-byte swizzle), so a K/V tile lands as
+// [8-key group][column half][8 rows][128 B]: a valid K-major operand (8-row atoms 2 KB
+// apart) for S and MN-major operand (column halves 1 KB apart) for P.V.
 //
-// Measured limit: a 128 x 128 x 16 tcgen05.mma issues in about the time of a
-// 128 x 256 x 16 one, so the 24 N = 128 MMAs per tile (8 for S, 16 for the hi + lo
-// P.V) set the pace; the softmax finishes inside that time.
+// Measured costs per 128-key tile on GB300 (clock64 traces and isolated probes): the
+// 24 N = 128 MMAs (8 for S, 16 for the hi + lo P.V) take the tensor pipe about 1700
+// cycles (64 each at full rate); the softmax of 128 rows about 1300 cycles on its four
+// warps.  The TMA producer spends about 100 cycles per box, so two 2 KB boxes per
+// block made it the bottleneck until one 4 KB box per block halved that.  A warp that
+// issues MMAs gets only the issue slots its scheduler's softmax warp leaves free
+// (every barrier poll then costs a few hundred cycles), which is why the issue loops
+// are short and why one serial S/P ring left the pipe idle half the time.
 //
-// Warp roles (192 threads): warps 0-3 softmax + epilogue (warp w owns TMEM lanes
-// 32w..32w+31), warp 4 TMA producer, warp 5 TMEM owner + MMA issuer.
-// TMEM columns: S/P buffers at [0, 128), [128, 256), [256, 384); O at [384, 512).
+// Warp roles (224 threads): warps 0-3 softmax + epilogue (warp w owns TMEM lanes
+// 32w..32w+31), warp 4 TMA producer, warp 5 TMEM owner + stream-0 issuer, warp 6
+// stream-1 issuer.  TMEM columns: S/P buffers of streams 0 and 1 at [0, 128) and
+// [128, 256); their O at [256, 384) and [384, 512).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,29 +67,30 @@ constexpr int kRows = 128;                 // query rows per tile
 constexpr int kKeys = 128;                 // keys per KV tile
 constexpr int kHead = 128;                 // head_dim
 constexpr int kBlk = 16;                   // tokens per pool block
-constexpr int kHalf = kRows * 128;         // one 64-column half of a 128-row tile: 16 KB
+constexpr int kHalf = kRows * 128;         // one 64-column half of the 128-row Q tile: 16 KB
 constexpr int kTileBytes = 2 * kHalf;      // 32 KB
-constexpr int kBoxBytes = kBlk * 128;      // one TMA box: 16 rows x 128 B
+constexpr int kBlockBytes = kBlk * 256;    // one pool block of one kv head: 16 rows x 256 B
+constexpr int kGroupBytes = 2048;          // K/V tiles: 8 rows x 2 halves x 128 B
 constexpr int kStagesK = 3;                // K stages: freed right after S = Q K^T
 constexpr int kStagesV = 3;                // V stages: freed after P.V
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileBytes;
 constexpr int kOffV = kOffK + kStagesK * kTileBytes;
 constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
-constexpr int kNumBars = 24;
+constexpr int kNumBars = 20;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1 KB alignment slack
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 192;
+constexpr int kMmaWarp = 5;                // issues stream 0 (even KV tiles); owns TMEM
+constexpr int kThreads = 224;              // warp 6 issues stream 1 (odd KV tiles)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 384;
-constexpr int kBufs = 3;                   // S/P buffers in TMEM
+constexpr uint32_t kTmemO = 256;           // O of stream s at kTmemO + 128 s
 constexpr float kLazyRescale = 8.0f;       // log2 units
+constexpr float kNoMax = -1.0e30f;         // running max before a stream saw a key
 
-// barrier indices
+// barrier indices: K/V stages (tile j uses stage j % 3), per-stream S/P buffer state.
 constexpr int BQ = 0, BK_FULL = 1, BK_EMPTY = 4, BV_FULL = 7, BV_EMPTY = 10, BS_FULL = 13,
-              BP_FULL = 16, BPV_DONE = 19;   // S_FULL / P_FULL / PV_DONE: one per buffer
+              BP_FULL = 15, BPV_DONE = 17;
 
 struct Ctl {
     uint64_t* bars;
@@ -84,31 +98,27 @@ struct Ctl {
     int* status;
 };
 
-// Bounded mbarrier wait shared by all roles: gives up when another role aborted
-// or after the time budget (then raises PKV_ERR_TIMEOUT and aborts the CTA).
-PKV_DEVINL bool wait_bar(const Ctl& c, int idx, uint32_t parity) {
+// Bounded mbarrier wait of a converged warp, shared by all roles: every lane polls and a
+// vote makes the outcome uniform (a completed phase stays completed), so the warp never
+// diverges; reconverging a diverged warp costs hundreds of cycles while the scheduler is
+// busy with the softmax.  Gives up when another role aborted or after the time budget
+// (then raises PKV_ERR_TIMEOUT and aborts the CTA).
+PKV_DEVINL bool wait_bar_warp(const Ctl& c, int idx, uint32_t parity, int lane) {
     uint64_t* bar = &c.bars[idx];
-    if (mbar_try_wait(bar, parity)) return true;
+    if (__any_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*c.abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitBudgetNs) {
-            raise_status(c.status, PKV_ERR_TIMEOUT);
-            *c.abort_flag = 1;
+        if (__any_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if (__any_sync(0xffffffffu, *c.abort_flag != 0)) return false;
+        if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > kWaitBudgetNs)) {
+            if (lane == 0) {
+                raise_status(c.status, PKV_ERR_TIMEOUT);
+                *c.abort_flag = 1;
+            }
+            __syncwarp();
             return false;
         }
     }
-}
-
-// Warp-uniform variant for the softmax warps: lane 0 polls, the result is broadcast,
-// and __syncwarp orders the other lanes after lane 0's acquire.
-PKV_DEVINL bool wait_bar_warp(const Ctl& c, int idx, uint32_t parity, int lane) {
-    int ok = 1;
-    if (lane == 0) ok = wait_bar(c, idx, parity) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
 }
 
 template <int G>
@@ -153,18 +163,16 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (warp == kMmaWarp) {
         if (lane == 0) {
             mbar_init(&bars[BQ], 1);
-            for (int s = 0; s < kStagesK; ++s) {
-                mbar_init(&bars[BK_FULL + s], 1);
-                mbar_init(&bars[BK_EMPTY + s], 1);
+            for (int st = 0; st < kStagesK; ++st) {
+                mbar_init(&bars[BK_FULL + st], 1);
+                mbar_init(&bars[BK_EMPTY + st], 1);
+                mbar_init(&bars[BV_FULL + st], 1);
+                mbar_init(&bars[BV_EMPTY + st], 1);
             }
-            for (int s = 0; s < kStagesV; ++s) {
-                mbar_init(&bars[BV_FULL + s], 1);
-                mbar_init(&bars[BV_EMPTY + s], 1);
-            }
-            for (int b = 0; b < kBufs; ++b) {
-                mbar_init(&bars[BS_FULL + b], 1);
-                mbar_init(&bars[BP_FULL + b], kSoftmaxWarps);
-                mbar_init(&bars[BPV_DONE + b], 1);
+            for (int sm = 0; sm < 2; ++sm) {
+                mbar_init(&bars[BS_FULL + sm], 1);
+                mbar_init(&bars[BP_FULL + sm], kSoftmaxWarps);
+                mbar_init(&bars[BPV_DONE + sm], 1);
             }
             *abort_flag = 0;
             fence_mbar_init();
@@ -186,7 +194,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         // ------------------------------------------------------------ TMA producer
         // The whole warp runs the loop: each lane prefetches one block id (32 ids =
         // 4 KV tiles per refill, independent loads), lane 0 sets the byte counts and
-        // lane b < 8 issues the boxes of block b of the tile.
+        // lane b < 8 issues the box of block b of the tile.
         const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
         const int nblk_needed = max_lim / kBlk + 1;
         if (lane == 0) {
@@ -213,78 +221,80 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 phys = 0;  // keep the byte count; the output is flagged invalid
             }
             const int row = (phys * a.num_kv_heads + kvh) * kBlk;
-            // K of tile jt: its stage is free once S of tile jt - kStagesK has run.
-            int ok = 1;
-            if (lane == 0 && jt >= kStagesK)
-                ok = wait_bar(ctl, BK_EMPTY + sk, ((jt / kStagesK) - 1) & 1);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(&bars[BK_FULL + sk], nb * 2 * kBoxBytes);
-            __syncwarp();
-            if (lane < nb) {
-                uint8_t* kdst = smem + kOffK + sk * kTileBytes + lane * kBoxBytes;
-                tma_load_2d(kdst, &tm_k, 0, row, &bars[BK_FULL + sk]);
-                tma_load_2d(kdst + kHalf, &tm_k, 64, row, &bars[BK_FULL + sk]);
-            }
+            // K of tile jt: its stage is free once S of tile jt - kStagesK has run.  The
+            // warp stays converged: lane 0 sets the byte count and lanes b < nb issue the
+            // boxes through predicated instructions.
+            if (jt >= kStagesK &&
+                !wait_bar_warp(ctl, BK_EMPTY + sk, ((jt / kStagesK) - 1) & 1, lane))
+                break;
+            mbar_arrive_expect_tx_if(lane == 0, &bars[BK_FULL + sk], nb * kBlockBytes);
+            tma_load_4d_if(lane < nb, smem + kOffK + sk * kTileBytes + lane * kBlockBytes, &tm_k,
+                           0, 0, 0, row / 8, &bars[BK_FULL + sk]);
             // V of tile jt: its stage is free once P.V of tile jt - kStagesV has run.
-            if (lane == 0 && jt >= kStagesV)
-                ok = wait_bar(ctl, BV_EMPTY + sv, ((jt / kStagesV) - 1) & 1);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(&bars[BV_FULL + sv], nb * 2 * kBoxBytes);
-            __syncwarp();
-            if (lane < nb) {
-                uint8_t* vdst = smem + kOffV + sv * kTileBytes + lane * kBoxBytes;
-                tma_load_2d(vdst, &tm_v, 0, row, &bars[BV_FULL + sv]);
-                tma_load_2d(vdst + kHalf, &tm_v, 64, row, &bars[BV_FULL + sv]);
-            }
-            __syncwarp();
+            if (jt >= kStagesV &&
+                !wait_bar_warp(ctl, BV_EMPTY + sv, ((jt / kStagesV) - 1) & 1, lane))
+                break;
+            mbar_arrive_expect_tx_if(lane == 0, &bars[BV_FULL + sv], nb * kBlockBytes);
+            tma_load_4d_if(lane < nb, smem + kOffV + sv * kTileBytes + lane * kBlockBytes, &tm_v,
+                           0, 0, 0, row / 8, &bars[BV_FULL + sv]);
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, kKeys, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, kHead, false, true);
-            const uint32_t tO = tmem + kTmemO;
-            bool ok = wait_bar(ctl, BQ, 0);
-            for (int jt = 0; ok && jt <= ntiles; ++jt) {
-                if (jt < ntiles) {
-                    // S_jt into buffer jt % 3, once P_{jt-3} in it has been consumed.
-                    const int ks_ = jt % kStagesK;
-                    const int sb = jt % kBufs;
-                    if (!wait_bar(ctl, BK_FULL + ks_, (jt / kStagesK) & 1)) break;
-                    if (jt >= kBufs && !wait_bar(ctl, BPV_DONE + sb, ((jt / kBufs) - 1) & 1))
-                        break;
-                    tc_fence_after();
-                    const uint32_t tS = tmem + sb * 128;
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // ------------------------------------------------------------ MMA issuers
+        // Stream sm = warp - kMmaWarp owns KV tiles j = sm, sm + 2, ...: S_j into its
+        // S/P buffer, then O_sm += P_j V_j once the softmax has written P_j there, then
+        // S_{j+2} into the same buffer once that P.V has completed.  Each stream is a
+        // serial chain, but the two interleave in the tensor pipe.  Each issuing warp
+        // shares its scheduler with a softmax warp and gets only the issue slots that
+        // warp leaves free, so the loop is short: the whole warp runs it converged (all
+        // lanes poll, then one leader lane issues through predicated instructions), and
+        // the descriptors are precomputed halves plus constant offsets.
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, kKeys, false, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, kHead, false, true);
+        constexpr uint32_t hi_q = smem_desc_sw128_hi(1024);          // Q: 8-row atoms 1 KB apart
+        constexpr uint32_t hi_kv = smem_desc_sw128_hi(kGroupBytes);  // K/V: 8-key groups 2 KB apart
+        const int sm = warp - kMmaWarp;
+        const uint32_t lo_q = smem_desc_sw128_lo(sQ, 16);
+        const uint32_t lo_k = smem_desc_sw128_lo(sK, 16);
+        const uint32_t lo_v = smem_desc_sw128_lo(sV, 1024);          // V: column halves 1 KB apart
+        const uint32_t tS = tmem + sm * 128;
+        const uint32_t tO = tmem + kTmemO + sm * 128;
+        const bool leader = elect_one();   // issues every MMA and commit of this stream
+        bool ok = wait_bar_warp(ctl, BQ, 0, lane);
+        for (int j = sm; ok && j < ntiles; j += 2) {
+            const int st = j % kStagesK;
+            const uint32_t use = static_cast<uint32_t>(j >> 1);   // this stream's tile count
+            // S_j: K_j landed, and P_{j-2} in the buffer consumed by its P.V.
+            if (!wait_bar_warp(ctl, BK_FULL + st, (j / kStagesK) & 1, lane)) break;
+            if (j >= 2 && !wait_bar_warp(ctl, BPV_DONE + sm, (use - 1) & 1, lane)) break;
+            tc_fence_after();
+            {
+                const uint32_t lk = lo_k + ((st * kTileBytes) >> 4);
 #pragma unroll
-                    for (int ks = 0; ks < kHead / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-                        umma_bf16(tS, smem_desc_sw128(sQ + off, 16, 1024),
-                                  smem_desc_sw128(sK + ks_ * kTileBytes + off, 16, 1024),
-                                  idesc_qk, ks > 0);
-                    }
-                    umma_commit(&bars[BS_FULL + sb]);
-                    umma_commit(&bars[BK_EMPTY + ks_]);
+                for (int ks = 0; ks < kHead / 16; ++ks) {
+                    const uint32_t kc = ((ks & 3) * 32) >> 4;   // 16 columns = 32 B
+                    umma_bf16_if(leader, tS,
+                                 desc_join(lo_q + (((ks >> 2) * kHalf) >> 4) + kc, hi_q),
+                                 desc_join(lk + (((ks >> 2) * 1024) >> 4) + kc, hi_kv), idesc_qk,
+                                 ks > 0);
                 }
-                if (jt >= 1) {
-                    const int j = jt - 1;
-                    const int pb = j % kBufs;
-                    const int vs = j % kStagesV;
-                    if (!wait_bar(ctl, BP_FULL + pb, (j / kBufs) & 1)) break;
-                    if (!wait_bar(ctl, BV_FULL + vs, (j / kStagesV) & 1)) break;
-                    tc_fence_after();
-                    const uint32_t tP = tmem + pb * 128;
+                umma_commit_if(leader, &bars[BS_FULL + sm]);
+                umma_commit_if(leader, &bars[BK_EMPTY + st]);
+            }
+            // O_sm += P_j V_j: P_j written, V_j landed.
+            if (!wait_bar_warp(ctl, BP_FULL + sm, use & 1, lane)) break;
+            if (!wait_bar_warp(ctl, BV_FULL + st, (j / kStagesV) & 1, lane)) break;
+            tc_fence_after();
+            {
+                const uint32_t lv = lo_v + ((st * kTileBytes) >> 4);
+                // V as the MN-major B operand: 16 keys = two 8-key groups.
 #pragma unroll
-                    for (int ks = 0; ks < kKeys / 16; ++ks) {
-                        const uint64_t bv =
-                            smem_desc_sw128(sV + vs * kTileBytes + ks * 2048, kHalf, 1024);
-                        umma_bf16_ta(tO, tP + ks * 8, bv, idesc_pv, (j > 0) || (ks > 0));
-                        umma_bf16_ta(tO, tP + 64 + ks * 8, bv, idesc_pv, true);
-                    }
-                    umma_commit(&bars[BPV_DONE + pb]);
-                    umma_commit(&bars[BV_EMPTY + vs]);
+                for (int ks = 0; ks < kKeys / 16; ++ks) {
+                    const uint64_t bv = desc_join(lv + ((ks * 2 * kGroupBytes) >> 4), hi_kv);
+                    umma_bf16_ta_if(leader, tO, tS + ks * 8, bv, idesc_pv, (j >= 2) || (ks > 0));
+                    umma_bf16_ta_if(leader, tO, tS + 64 + ks * 8, bv, idesc_pv, true);
                 }
+                umma_commit_if(leader, &bars[BPV_DONE + sm]);
+                umma_commit_if(leader, &bars[BV_EMPTY + st]);
             }
         }
     } else {
@@ -296,13 +306,15 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         const bool row_valid = tok < n;
         const int lim = cascade ? c - 1 : (row_valid ? c + tok : c + n - 1);  // last key seen
         const float sl2 = a.scale_log2;
-        float m_used = -INFINITY;
-        float l = 0.f;
+        // Running max (log2 domain) and row sum of each stream: even and odd KV tiles
+        // accumulate into separate O buffers and are merged after the last tile.
+        float m_st[2] = {kNoMax, kNoMax};
+        float l_st[2] = {0.f, 0.f};
         bool ok = true;
         for (int jt = 0; jt < ntiles; ++jt) {
-            const int b = jt % kBufs;
-            const uint32_t tS = tmem + lane_addr + b * 128;
-            if (!wait_bar_warp(ctl, BS_FULL + b, (jt / kBufs) & 1, lane)) { ok = false; break; }
+            const int sm = jt & 1;
+            const uint32_t tS = tmem + lane_addr + sm * 128;
+            if (!wait_bar_warp(ctl, BS_FULL + sm, (jt >> 1) & 1, lane)) { ok = false; break; }
             tc_fence_after();
             float x[kKeys];
 #pragma unroll
@@ -311,33 +323,32 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             tmem_wait_ld();
 
             const int kbase = jt * kKeys;
-            // Row max over 8 independent chains (one softmax warp per scheduler has
-            // no other warp to hide long dependency chains behind).
-            float m8[8];
+            if (kbase + kKeys - 1 > lim) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
-            if (kbase + kKeys - 1 <= lim) {
-#pragma unroll
-                for (int k = 0; k < kKeys; ++k) m8[k & 7] = fmaxf(m8[k & 7], x[k]);
-            } else {
-#pragma unroll
-                for (int k = 0; k < kKeys; ++k) {
-                    x[k] = (kbase + k <= lim) ? x[k] : -INFINITY;
-                    m8[k & 7] = fmaxf(m8[k & 7], x[k]);
-                }
+                for (int k = 0; k < kKeys; ++k) x[k] = (kbase + k <= lim) ? x[k] : -INFINITY;
             }
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            // Row max over 4 independent chains of three-input max (one softmax warp per
+            // scheduler has no other warp to hide long dependency chains behind).
+            float m4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) m4[u] = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kKeys; k += 2)
+                m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], x[k], x[k + 1]);
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             const float m_tile = mx * sl2;   // scale > 0: max commutes with scaling
+            // (sm is warp-uniform: selects, not indexed register arrays)
+            const float m_used = sm ? m_st[1] : m_st[0];
             const bool grow = m_tile > m_used + kLazyRescale;
             const float m_cur = grow ? m_tile : m_used;
-            const float alpha = fast_exp2(m_used - m_cur);   // 1 unless grow; 0 at start
-            // O is rescaled only when some row of the warp grew its max; that needs the
-            // previous tile's P.V to have finished.  Otherwise P.V of tile jt - 1 keeps
-            // running while this tile's P is written to its own buffer.
-            if (jt >= 1 && __any_sync(0xffffffffu, grow)) {
-                if (!wait_bar_warp(ctl, BPV_DONE + (jt - 1) % kBufs, ((jt - 1) / kBufs) & 1,
-                                   lane)) {
+            // 1 unless grow; 0 when the stream had no key yet.  A row with no key in
+            // this tile keeps m_cur finite (kNoMax at worst), so its p are exp2(-inf) = 0.
+            const float alpha = fast_exp2(m_used - m_cur);
+            // O_sm is rescaled only when some row of the warp grew its max.  The stream's
+            // previous P.V (tile jt - 2) has completed already: S_jt waited for it before
+            // overwriting the buffer; the wait below only makes that visible here.
+            if (jt >= 2 && __any_sync(0xffffffffu, grow)) {
+                if (!wait_bar_warp(ctl, BPV_DONE + sm, ((jt >> 1) - 1) & 1, lane)) {
                     ok = false;
                     break;
                 }
@@ -345,7 +356,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float o[32];
-                    const uint32_t ta = tmem + lane_addr + kTmemO + q * 32;
+                    const uint32_t ta = tmem + lane_addr + kTmemO + sm * 128 + q * 32;
                     tmem_ld32(ta, o);
                     tmem_wait_ld();
 #pragma unroll
@@ -355,7 +366,9 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             // P_jt over S_jt in the same buffer (S is already in registers): hi in columns
             // [0, 64), lo in [64, 128), written 32 keys at a time so that few packed
-            // values are live and the exp chains of a chunk overlap.
+            // values are live and the exp chains of a chunk overlap.  hi is p truncated
+            // to bf16, lo the exact remainder p - hi truncated to bf16: hi + lo is within
+            // 2^-14 of p (relative), from byte permutes instead of conversions.
             float rs8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
@@ -365,20 +378,30 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int k = q * 32 + 2 * e;
-                    const float p0 = fast_exp2(fmaf(x[k], sl2, -m_cur));
-                    const float p1 = fast_exp2(fmaf(x[k + 1], sl2, -m_cur));
-                    rs8[e & 7] += p0 + p1;
-                    const uint32_t h = pack_bf16x2(p0, p1);
-                    phi[e] = h;
-                    plo[e] = pack_bf16x2(p0 - bf16lo_to_f32(h), p1 - bf16hi_to_f32(h));
+                    float a0, a1;
+                    ffma2(a0, a1, x[k], x[k + 1], sl2, sl2, -m_cur, -m_cur);
+                    const float p0 = fast_exp2(a0);
+                    const float p1 = fast_exp2(a1);
+                    const int u = (e & 3) * 2;
+                    fadd2(rs8[u], rs8[u + 1], rs8[u], rs8[u + 1], p0, p1);
+                    phi[e] = pack_bf16x2_trunc(p0, p1);
+                    float r0, r1;
+                    ffma2(r0, r1, __uint_as_float(__float_as_uint(p0) & 0xffff0000u),
+                          __uint_as_float(__float_as_uint(p1) & 0xffff0000u), -1.f, -1.f, p0, p1);
+                    plo[e] = pack_bf16x2_trunc(r0, r1);
                 }
                 tmem_st16(tS + q * 16, phi);
                 tmem_st16(tS + 64 + q * 16, plo);
             }
             const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
                              ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-            l = l * alpha + rs;
-            m_used = m_cur;
+            if (sm) {
+                l_st[1] = l_st[1] * alpha + rs;
+                m_st[1] = m_cur;
+            } else {
+                l_st[0] = l_st[0] * alpha + rs;
+                m_st[0] = m_cur;
+            }
             tmem_wait_st();
             // Keys past the last one this tile needs are masked for every row, but their
             // V rows may hold anything (NaN in unused slots, stale data where no block was
@@ -390,52 +413,70 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                     break;
                 }
                 if (kbase + row > max_lim) {
-                    uint8_t* vrow = smem + kOffV + (jt % kStagesV) * kTileBytes + row * 128;
+                    uint8_t* vrow = smem + kOffV + (jt % kStagesV) * kTileBytes +
+                                    (row >> 3) * kGroupBytes + (row & 7) * 128;
                     const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         *reinterpret_cast<uint4*>(vrow + (j << 4)) = z;
-                        *reinterpret_cast<uint4*>(vrow + kHalf + (j << 4)) = z;
+                        *reinterpret_cast<uint4*>(vrow + 1024 + (j << 4)) = z;
                     }
                 }
                 fence_proxy_async_smem();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[BP_FULL + b]);
+            mbar_arrive_if(lane == 0, &bars[BP_FULL + sm]);
         }
         // ------------------------------------------------------------ epilogue
-        if (ok && wait_bar_warp(ctl, BPV_DONE + (ntiles - 1) % kBufs,
-                                ((ntiles - 1) / kBufs) & 1, lane)) {
+        // Merge the streams: with a_s = 2^(m_s - m), m = max(m_0, m_1),
+        //   O = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1).
+        // Stream 0 always holds key 0, which every row sees, so m_0 and l_0 are proper.
+        const int n0 = (ntiles + 1) >> 1, n1 = ntiles >> 1;   // tiles of each stream
+        bool fin = ok && wait_bar_warp(ctl, BPV_DONE + 0, (n0 - 1) & 1, lane);
+        if (fin && n1 > 0) fin = wait_bar_warp(ctl, BPV_DONE + 1, (n1 - 1) & 1, lane);
+        if (fin) {
             tc_fence_after();
-            const float inv_l = 1.f / l;
+            const float m = fmaxf(m_st[0], m_st[1]);
+            const float a0 = fast_exp2(m_st[0] - m);
+            const float a1 = n1 > 0 ? fast_exp2(m_st[1] - m) : 0.f;
+            const float lsum = a0 * l_st[0] + a1 * l_st[1];
+            const float c0 = a0 / lsum, c1 = a1 / lsum;
             const size_t orow_idx = static_cast<size_t>(qoff + tok) * a.num_q_heads + head;
             uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * kHead;
             const size_t prow = orow_idx * a.max_parts_total;   // cascade: partition 0
             if (cascade && row_valid) {
-                a.m_part[prow] = m_used;   // log2 domain, as the decode partials
-                a.l_part[prow] = l;
+                a.m_part[prow] = m;   // log2 domain, as the decode partials
+                a.l_part[prow] = lsum;
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float o[32];
                 tmem_ld32(tmem + lane_addr + kTmemO + q * 32, o);
                 tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] *= c0;
+                if (n1 > 0) {
+                    float o1[32];
+                    tmem_ld32(tmem + lane_addr + kTmemO + 128 + q * 32, o1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = fmaf(o1[e], c1, o[e]);
+                }
                 if (cascade && row_valid) {
                     float* dst = a.o_part + prow * kHead + q * 32;
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
                         *reinterpret_cast<float4*>(dst + e) =
-                            make_float4(o[e] * inv_l, o[e + 1] * inv_l, o[e + 2] * inv_l,
-                                        o[e + 3] * inv_l);
+                            make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
                 } else if (row_valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         uint4 w;
-                        w.x = pack_bf16x2(o[e] * inv_l, o[e + 1] * inv_l);
-                        w.y = pack_bf16x2(o[e + 2] * inv_l, o[e + 3] * inv_l);
-                        w.z = pack_bf16x2(o[e + 4] * inv_l, o[e + 5] * inv_l);
-                        w.w = pack_bf16x2(o[e + 6] * inv_l, o[e + 7] * inv_l);
+                        w.x = pack_bf16x2(o[e], o[e + 1]);
+                        w.y = pack_bf16x2(o[e + 2], o[e + 3]);
+                        w.z = pack_bf16x2(o[e + 4], o[e + 5]);
+                        w.w = pack_bf16x2(o[e + 6], o[e + 7]);
                         *reinterpret_cast<uint4*>(orow + q * 32 + e) = w;
                     }
                 }
@@ -457,7 +498,7 @@ cudaError_t launch_g(const PrefillArgs& a, cudaStream_t stream) {
     CUtensorMap mq, mk, mv;
     const int64_t rows = a.num_blocks * a.num_kv_heads * kBlk;
     if (!make_q_group_map(&mq, a.q, a.total_new, a.num_q_heads, kHead, G, kRows / G) ||
-        !make_pool_map(&mk, a.k_pool, rows, kHead) || !make_pool_map(&mv, a.v_pool, rows, kHead))
+        !make_pool_block_map(&mk, a.k_pool, rows) || !make_pool_block_map(&mv, a.v_pool, rows))
         return cudaErrorInvalidValue;
     auto kern = prefill_tcgen05_kernel<G>;
     cudaError_t e =

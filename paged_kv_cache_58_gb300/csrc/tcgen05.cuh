@@ -61,6 +61,38 @@ PKV_DEVINL void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, 
         : "memory");
 }
 
+// Predicated forms (only the lane with `on` issues) for a converged issuing warp.
+PKV_DEVINL void umma_bf16_if(bool on, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                             uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u),
+        "r"(static_cast<uint32_t>(on))
+        : "memory");
+}
+
+PKV_DEVINL void umma_bf16_ta_if(bool on, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u),
+        "r"(static_cast<uint32_t>(on))
+        : "memory");
+}
+
+PKV_DEVINL void umma_commit_if(bool on, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar)),
+        "r"(static_cast<uint32_t>(on))
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 PKV_DEVINL void umma_commit(uint64_t* bar) {
@@ -94,6 +126,19 @@ PKV_DEVINL uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) 
     d |= 1ull << 46;
     d |= 2ull << 61;
     return d;
+}
+
+// The same descriptor as two 32-bit halves, so that per-MMA offsets are one 32-bit add
+// on the low half (start address field, bits 0-13; shared-memory addresses stay below
+// 2^18, so the field never carries into the leading-offset field).
+PKV_DEVINL uint32_t smem_desc_sw128_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t smem_desc_sw128_hi(uint32_t sbo) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+PKV_DEVINL uint64_t desc_join(uint32_t lo, uint32_t hi) {
+    return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 // ------------------------------------------------------------------ TMEM <-> registers

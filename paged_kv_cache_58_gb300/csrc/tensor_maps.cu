@@ -41,6 +41,20 @@ bool make_pool_map(CUtensorMap* m, const void* pool, int64_t rows, int head_dim)
            CUDA_SUCCESS;
 }
 
+bool make_pool_block_map(CUtensorMap* m, const void* pool, int64_t rows) {
+    auto fn = encode_fn();
+    if (!fn || rows % 8 != 0) return false;
+    // Row r of the pool starts at r * 256 bytes; its column half h at + h * 128.
+    cuuint64_t dims[4] = {64, 8, 2, static_cast<cuuint64_t>(rows / 8)};
+    cuuint64_t strides[3] = {256, 128, 8 * 256};
+    cuuint32_t box[4] = {64, 8, 2, 2};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 bool make_q_group_map(CUtensorMap* m, const void* q, int tokens, int hq, int head_dim, int G,
                       int tok) {
     auto fn = encode_fn();
