@@ -105,6 +105,21 @@ PKV_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
     }
 }
 
+// Bounded wait of a converged warp: every lane polls and a vote makes the outcome
+// uniform (a completed phase stays completed), so the warp never diverges.
+PKV_DEVINL bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status) {
+    if (__any_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (__any_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > kWaitBudgetNs)) {
+            if ((threadIdx.x & 31) == 0) raise_status(status, PKV_ERR_TIMEOUT);
+            __syncwarp();
+            return false;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ async copies
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
 // both addresses 16-byte aligned).
@@ -142,6 +157,16 @@ PKV_DEVINL void tma_load_4d(void* smem_dst, const void* tmap, int32_t x, int32_t
         "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
+PKV_DEVINL void tma_load_2d_if(bool on, void* smem_dst, const void* tmap, int32_t x, int32_t y,
+                               uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n\t}" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "r"(static_cast<uint32_t>(on))
         : "memory");
 }
 

@@ -18,8 +18,12 @@
 // wrong orientation and is transposed in registers with movmatrix; it is split into
 // bf16 hi + lo parts so the probabilities keep ~2^-17 relative precision.
 //
-// Staging: each block's K and V slabs arrive as TMA boxes of 16 rows x 64 columns
-// with the 128-byte swizzle, so ldmatrix reads them without bank conflicts.
+// Staging: each block's K slab and V slab arrive as one TMA box each, with the 128-byte
+// swizzle so that ldmatrix reads them without bank conflicts: for head_dim 128 a 4-D
+// box (the block's 16 rows x 256 B as 2 row groups x 2 column halves x 8 rows x 128 B),
+// for head_dim 64 a 16-row x 64-column box.  The warp stays converged throughout: the
+// stage waits vote across lanes and the copies are predicated, because reconverging a
+// diverged warp costs hundreds of cycles on a busy scheduler.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -34,7 +38,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;
 constexpr int kBlk = 16;
-constexpr int kBox = kBlk * 128;  // one 16-row x 64-column bf16 box
+constexpr int kAtom = 8 * 128;    // 8 rows x 128 B: one swizzle atom
 constexpr float kLazyRescale = 8.0f;
 
 PKV_DEVINL void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -64,15 +68,18 @@ PKV_DEVINL void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, u
 }
 
 // Address of 16-byte chunk `c` (0 .. D/8-1) of row `t` (0..15) of a slab staged as
-// D/64 boxes of 2048 B with the 128-byte swizzle (chunk index XOR row % 8).
+// [row group t/8][column half c/8][8 rows][128 B] with the 128-byte swizzle (chunk
+// index XOR row % 8).
+template <int D>
 PKV_DEVINL uint32_t slab_addr(uint32_t base, int t, int c) {
-    return base + (c >> 3) * kBox + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+    return base + (t >> 3) * (D / 64) * kAtom + (c >> 3) * kAtom + (t & 7) * 128 +
+           (((c & 7) ^ (t & 7)) << 4);
 }
 
 template <int D, int G>
 struct TcSmem {
     static constexpr int kHalves = D / 64;
-    static constexpr int kSlab = kHalves * kBox;          // K or V slab of one block
+    static constexpr int kSlab = kBlk * D * 2;            // K or V slab of one block
     static constexpr int kStageBytes = 2 * kSlab;
     static constexpr int kRing = kWarps * kStages * kStageBytes;
     // merge scratch reuses the ring once every warp is done
@@ -117,7 +124,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kRing) + warp * kStages;
     const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.max_blocks_per_seq;
 
-    if (lane == 0) {
+    if (lane == 0) {   // once per CTA
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
 #pragma unroll
@@ -134,28 +141,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     };
     fetch_ids(0);
 
-    auto issue = [&](int i, int phys) {  // lane 0 only
+    // Stage i: lane 0 sets the byte count, lane 0 copies the K slab and lane 1 the V
+    // slab; all lanes execute the predicated instructions (no branch).
+    auto issue = [&](int i, int phys, bool on) {
         uint8_t* st = ring + (i % kStages) * SM::kStageBytes;
         uint64_t* bar = &bars[i % kStages];
-        if (phys < 0 || phys >= a.num_blocks) {
-            raise_status(a.status, PKV_ERR_OOB);
-            mbar_arrive(bar);  // complete the phase without data; output is invalid
-            return;
-        }
-        const int row = (phys * a.num_kv_heads + kvh) * kBlk;
-        mbar_arrive_expect_tx(bar, SM::kStageBytes);
-#pragma unroll
-        for (int h = 0; h < SM::kHalves; ++h) {
-            tma_load_2d(st + h * kBox, &tm_k, 64 * h, row, bar);
-            tma_load_2d(st + SM::kSlab + h * kBox, &tm_v, 64 * h, row, bar);
-        }
+        const bool bad = phys < 0 || phys >= a.num_blocks;
+        if (on && bad && lane == 0) raise_status(a.status, PKV_ERR_OOB);
+        mbar_arrive_if(on && bad && lane == 0, bar);  // complete the phase without data
+        const int row = (bad ? kvh : phys * a.num_kv_heads + kvh) * kBlk;
+        mbar_arrive_expect_tx_if(on && !bad && lane == 0, bar, SM::kStageBytes);
+        const bool mine = on && !bad && lane < 2;
+        uint8_t* dst = st + (lane == 1 ? SM::kSlab : 0);
+        const void* map = lane == 1 ? static_cast<const void*>(&tm_v) : &tm_k;
+        if constexpr (D == 128)
+            tma_load_4d_if(mine, dst, map, 0, 0, 0, row / 8, bar);
+        else
+            tma_load_2d_if(mine, dst, map, 0, row, bar);
     };
 
 #pragma unroll
-    for (int i = 0; i < kStages; ++i) {
-        const int id = __shfl_sync(0xffffffffu, ids, i);
-        if (lane == 0 && i < my_count) issue(i, id);
-    }
+    for (int i = 0; i < kStages; ++i) issue(i, __shfl_sync(0xffffffffu, ids, i), i < my_count);
 
     // q^T as the B operand of the score MMA: lane holds head lane/4 (zero if >= G),
     // dims 16ks + 2(lane%4) + {0,1} (b0) and +8 (b1).
@@ -200,7 +206,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     int failed_at = -1;
     for (int i = 0; i < my_count; ++i) {
         const int st_i = i % kStages;
-        if (!mbar_wait(&bars[st_i], (i / kStages) & 1, a.status)) {
+        if (!mbar_wait_warp(&bars[st_i], (i / kStages) & 1, a.status)) {
             failed_at = i;
             break;
         }
@@ -216,7 +222,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             for (int idx = lane; idx < (kBlk - valid) * SM::kHalves * 8; idx += 32) {
                 const int t = valid + idx / (SM::kHalves * 8);
                 const int c = idx % (SM::kHalves * 8);
-                *reinterpret_cast<uint4*>(vrows + (c >> 3) * kBox + t * 128 + ((c & 7) << 4)) =
+                *reinterpret_cast<uint4*>(vrows + (t >> 3) * SM::kHalves * kAtom +
+                                          (c >> 3) * kAtom + (t & 7) * 128 + ((c & 7) << 4)) =
                     make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
@@ -228,7 +235,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4(slab_addr(kbase, k_tok, 2 * ks + k_chk), a0, a1, a2, a3);
+            ldsm_x4(slab_addr<D>(kbase, k_tok, 2 * ks + k_chk), a0, a1, a2, a3);
             mma_bf16(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
         }
 #pragma unroll
@@ -278,19 +285,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(slab_addr(vbase, v_tok, 2 * mt + v_chk), a0, a1, a2, a3);
+            ldsm_x4_t(slab_addr<D>(vbase, v_tok, 2 * mt + v_chk), a0, a1, a2, a3);
             mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
             mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
         }
         __syncwarp();
         const int nxt = i + kStages;
         if ((nxt & 31) == 0 && nxt < my_count) fetch_ids(nxt);
-        const int id = __shfl_sync(0xffffffffu, ids, nxt & 31);
-        if (lane == 0 && nxt < my_count) issue(nxt, id);
+        issue(nxt, __shfl_sync(0xffffffffu, ids, nxt & 31), nxt < my_count);
     }
     if (failed_at >= 0) {
         for (int j = failed_at + 1; j < my_count && j < failed_at + kStages; ++j)
-            mbar_wait(&bars[j % kStages], (j / kStages) & 1, a.status);
+            mbar_wait_warp(&bars[j % kStages], (j / kStages) & 1, a.status);
     }
 
     // full denominators of h0, h1 over this warp's tokens
@@ -355,8 +361,11 @@ cudaError_t launch_tc(const DecodeArgs& a, cudaStream_t stream) {
     using SM = TcSmem<D, G>;
     CUtensorMap mk, mv;
     const int64_t rows = a.num_blocks * a.num_kv_heads * kBlk;
-    if (!make_pool_map(&mk, a.k_pool, rows, D) || !make_pool_map(&mv, a.v_pool, rows, D))
-        return cudaErrorInvalidValue;
+    const bool maps_ok = D == 128 ? make_pool_block_map(&mk, a.k_pool, rows) &&
+                                        make_pool_block_map(&mv, a.v_pool, rows)
+                                  : make_pool_map(&mk, a.k_pool, rows, D) &&
+                                        make_pool_map(&mv, a.v_pool, rows, D);
+    if (!maps_ok) return cudaErrorInvalidValue;
     auto kern = decode_tc_kernel<D, G>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
