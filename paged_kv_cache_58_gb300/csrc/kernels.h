@@ -118,6 +118,9 @@ struct PrefillArgs {
     float* o_part;
     float* m_part;
     float* l_part;
+    // A CTA whose rows all attend at least this many keys stores P as one bf16 value
+    // (round to nearest); otherwise as bf16 hi + lo (see the prefill kernel).
+    int p_single_min_keys;
 };
 
 cudaError_t launch_paged_prefill(const PrefillArgs& a, int group, cudaStream_t stream);

@@ -21,7 +21,12 @@
 //                  from shared memory) into the TMEM accumulator O of stream j % 2
 // The split keeps the probabilities near fp32 precision: a single bf16 P is off by up
 // to 2^-8 per weight, which rows attending only a few keys do not average away; with
-// the split every output is within 2^-14 * max|v| of the exact weights' result.
+// the split every output is within 2^-14 * max|v| of the exact weights' result.  A
+// tile whose rows all attend at least p_single_min_keys keys (1024 by default) keeps a
+// single bf16 P, rounded to nearest, as FlashAttention-style kernels do: there the
+// rounding errors of many weights average out (for N(0,1) data their effect on an
+// output has a standard deviation near 2^-8 / sqrt(3 n / e) for n keys, about 1.2e-4
+// at n = 1024), and the P.V pass takes 8 MMAs instead of 16.
 // The running max is updated lazily: O and l are rescaled only when a row's max
 // grows by more than 2^8, which keeps P <= 256 and leaves the result exact.
 //
@@ -154,6 +159,9 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int ntiles = max_lim / kKeys + 1;
     const int qoff = cascade ? 0 : a.q_offsets[r];
     const int qrow0 = qoff + t0;             // first token row of the tile in q / out
+    // Every row of the tile attends at least min_keys keys (its first token the fewest).
+    const int min_keys = cascade ? c : c + t0 + 1;
+    const bool p_single = min_keys >= a.p_single_min_keys;   // uniform over the CTA
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
@@ -291,7 +299,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 for (int ks = 0; ks < kKeys / 16; ++ks) {
                     const uint64_t bv = desc_join(lv + ((ks * 2 * kGroupBytes) >> 4), hi_kv);
                     umma_bf16_ta_if(leader, tO, tS + ks * 8, bv, idesc_pv, (j >= 2) || (ks > 0));
-                    umma_bf16_ta_if(leader, tO, tS + 64 + ks * 8, bv, idesc_pv, true);
+                    if (!p_single) umma_bf16_ta_if(leader, tO, tS + 64 + ks * 8, bv, idesc_pv, true);
                 }
                 umma_commit_if(leader, &bars[BPV_DONE + sm]);
                 umma_commit_if(leader, &bars[BV_EMPTY + st]);
@@ -372,6 +380,25 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             float rs8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+            if (p_single) {
+                // One bf16 P per weight (round to nearest) in columns [0, 64).
+#pragma unroll
+                for (int q = 0; q < kKeys / 32; ++q) {
+                    uint32_t ph[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int k = q * 32 + 2 * e;
+                        float a0, a1;
+                        ffma2(a0, a1, x[k], x[k + 1], sl2, sl2, -m_cur, -m_cur);
+                        const float p0 = fast_exp2(a0);
+                        const float p1 = fast_exp2(a1);
+                        const int u = (e & 3) * 2;
+                        fadd2(rs8[u], rs8[u + 1], rs8[u], rs8[u + 1], p0, p1);
+                        ph[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tS + q * 16, ph);
+                }
+            } else {
 #pragma unroll
             for (int q = 0; q < kKeys / 32; ++q) {
                 uint32_t phi[16], plo[16];
@@ -392,6 +419,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
                 tmem_st16(tS + q * 16, phi);
                 tmem_st16(tS + 64 + q * 16, plo);
+            }
             }
             const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
                              ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));

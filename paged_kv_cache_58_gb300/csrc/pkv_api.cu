@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -83,6 +84,16 @@ int auto_partition(int num_seqs, int num_q_heads, int max_context) {
 bool decode_use_simt() {
     const char* v = std::getenv("PKV_DECODE_KERNEL");
     return v != nullptr && std::strcmp(v, "simt") == 0;
+}
+
+// Prefill probabilities: one bf16 value per weight for query tiles whose rows all
+// attend at least kPSingleMinKeys keys, the exact hi + lo split below that;
+// PKV_PREFILL_P=split forces the split everywhere (read at each call; used to test and
+// compare the two).
+constexpr int kPSingleMinKeys = 1024;
+int prefill_p_single_min_keys() {
+    const char* v = std::getenv("PKV_PREFILL_P");
+    return (v != nullptr && std::strcmp(v, "split") == 0) ? INT_MAX : kPSingleMinKeys;
 }
 
 size_t decode_workspace(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
@@ -345,6 +356,7 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
     pa.cascade_keys = prefix_len;
     pa.cascade_rows = num_seqs;
     pa.max_parts_total = parts + 1;
+    pa.p_single_min_keys = prefill_p_single_min_keys();
     pa.o_part = o_part;
     pa.m_part = m_part;
     pa.l_part = l_part;
@@ -419,6 +431,7 @@ pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = pool->num_kv_heads;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    a.p_single_min_keys = prefill_p_single_min_keys();
     const cudaError_t e = pkv::launch_paged_prefill(a, group, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
     return from_cuda(e);

@@ -72,6 +72,24 @@ def test_prefill_edges(pkv, oracle_mod, cached, new):
     check_attention(run_prefill(pkv, case), ref)
 
 
+def test_prefill_p_modes_long_rows(pkv, oracle_mod, monkeypatch):
+    """Query tiles whose rows all attend >= 1024 keys keep a single bf16 P by default;
+    PKV_PREFILL_P=split forces the hi + lo split.  Both meet the tolerance on the same
+    long-context case, and the split is closer to the oracle in RMS (its weights differ
+    from the exact ones by 2^-14 instead of 2^-8)."""
+    case = custom_case(32, 8, [1500, 3000], [200, 129], seed=11)
+    ref, _, _ = oracle_prefill_case(oracle_mod, case)
+    monkeypatch.delenv("PKV_PREFILL_P", raising=False)
+    single = run_prefill(pkv, case)
+    check_attention(single, ref)
+    monkeypatch.setenv("PKV_PREFILL_P", "split")
+    split = run_prefill(pkv, case)
+    check_attention(split, ref)
+    assert not torch.equal(single, split), "both runs took the same P path"
+    rms = lambda t: float(np.sqrt(np.mean((t.double().cpu().numpy() - ref) ** 2)))
+    assert rms(split) < rms(single)
+
+
 def test_prefill_last_row_equals_decode(pkv, oracle_mod):
     """The last prefill row of a request equals a decode of that token (two kernels)."""
     case = custom_case(32, 8, [700], [40], seed=5)
