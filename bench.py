@@ -174,10 +174,18 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def kernel_traffic(kernel_src: str, summary: str):
-    """DRAM bytes per launch recorded by an ncu capture of this exact kernel source."""
+# Files the tensor-core decode kernel is compiled from (its ncu record names their sha1).
+DECODE_TC_SOURCES = ("paged_decode_tc.cu", "common.cuh", "kernels.h")
+
+
+def kernel_traffic(kernel_srcs, summary: str):
+    """DRAM bytes per launch recorded by an ncu capture of exactly these kernel sources
+    (sha1 over the files in order); None once any of them changed."""
     try:
-        digest = hashlib.sha1(open(kernel_src, "rb").read()).hexdigest()[:12]
+        h = hashlib.sha1()
+        for f in kernel_srcs:
+            h.update(open(f, "rb").read())
+        digest = h.hexdigest()[:12]
         text = open(summary).read()
     except OSError:
         return None
@@ -451,8 +459,8 @@ def main():
     achieved = unique_bytes / (decode_ms * 1e-3) / 1e9
     traffic = None
     if args.workload == "8b" and case.q.dtype.itemsize == 2:
-        traffic = kernel_traffic(os.path.join(ROOT, "paged_kv_cache_58_gb300", "csrc",
-                                              "paged_decode_tc.cu"),
+        csrc = os.path.join(ROOT, "paged_kv_cache_58_gb300", "csrc")
+        traffic = kernel_traffic([os.path.join(csrc, f) for f in DECODE_TC_SOURCES],
                                  os.path.join(ROOT, "profiles", "paged_decode_tc_llama3_8b.md"))
     prefill = None
     if not args.no_prefill:
