@@ -82,7 +82,7 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileBytes;
 constexpr int kOffV = kOffK + kStagesK * kTileBytes;
 constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
-constexpr int kNumBars = 20;
+constexpr int kNumBars = 21;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1 KB alignment slack
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
@@ -95,7 +95,7 @@ constexpr float kNoMax = -1.0e30f;         // running max before a stream saw a 
 
 // barrier indices: K/V stages (tile j uses stage j % 3), per-stream S/P buffer state.
 constexpr int BQ = 0, BK_FULL = 1, BK_EMPTY = 4, BV_FULL = 7, BV_EMPTY = 10, BS_FULL = 13,
-              BP_FULL = 15, BPV_DONE = 17;
+              BP_FULL = 15, BPV_DONE = 17, BDRAIN = 19;   // BDRAIN: per stream, at exit
 
 struct Ctl {
     uint64_t* bars;
@@ -181,6 +181,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 mbar_init(&bars[BS_FULL + sm], 1);
                 mbar_init(&bars[BP_FULL + sm], kSoftmaxWarps);
                 mbar_init(&bars[BPV_DONE + sm], 1);
+                mbar_init(&bars[BDRAIN + sm], 1);
             }
             *abort_flag = 0;
             fence_mbar_init();
@@ -214,6 +215,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             tma_load_3d(smem + kOffQ + kHalf, &tm_q, 64, kvh * G, qrow0, &bars[BQ]);
         }
         int ids = 0;
+        int k_issued = 0, v_issued = 0;   // tiles whose K / V copies were issued
         for (int jt = 0; jt < ntiles; ++jt) {
             constexpr int kPerTile = kKeys / kBlk;   // 8 blocks per KV tile
             if ((jt & 3) == 0) {
@@ -238,6 +240,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_arrive_expect_tx_if(lane == 0, &bars[BK_FULL + sk], nb * kBlockBytes);
             tma_load_4d_if(lane < nb, smem + kOffK + sk * kTileBytes + lane * kBlockBytes, &tm_k,
                            0, 0, 0, row / 8, &bars[BK_FULL + sk]);
+            ++k_issued;
             // V of tile jt: its stage is free once P.V of tile jt - kStagesV has run.
             if (jt >= kStagesV &&
                 !wait_bar_warp(ctl, BV_EMPTY + sv, ((jt / kStagesV) - 1) & 1, lane))
@@ -245,6 +248,21 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_arrive_expect_tx_if(lane == 0, &bars[BV_FULL + sv], nb * kBlockBytes);
             tma_load_4d_if(lane < nb, smem + kOffV + sv * kTileBytes + lane * kBlockBytes, &tm_v,
                            0, 0, 0, row / 8, &bars[BV_FULL + sv]);
+            ++v_issued;
+        }
+        // Drain (also after an abort): wait, bounded, until the last copy issued into
+        // every stage has landed, so that no TMA write into shared memory outlives the
+        // CTA.  No later copy goes into those stages, so the phases cannot move on.
+        mbar_wait_warp(&bars[BQ], 0, a.status);
+        for (int st = 0; st < kStagesK; ++st) {
+            if (k_issued > st) {
+                const int last = st + kStagesK * ((k_issued - 1 - st) / kStagesK);
+                mbar_wait_warp(&bars[BK_FULL + st], (last / kStagesK) & 1, a.status);
+            }
+            if (v_issued > st) {
+                const int last = st + kStagesV * ((v_issued - 1 - st) / kStagesV);
+                mbar_wait_warp(&bars[BV_FULL + st], (last / kStagesV) & 1, a.status);
+            }
         }
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
         // ------------------------------------------------------------ MMA issuers
@@ -305,6 +323,10 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 umma_commit_if(leader, &bars[BV_EMPTY + st]);
             }
         }
+        // Drain (also after an abort): every MMA this stream issued completes before
+        // the TMEM is freed at the end of the kernel.
+        umma_commit_if(leader, &bars[BDRAIN + sm]);
+        mbar_wait_warp(&bars[BDRAIN + sm], 0, a.status);
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         const int row = threadIdx.x;              // 0..127 == TMEM lane
