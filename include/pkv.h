@@ -16,8 +16,9 @@
  *      k_pool, v_pool: [num_blocks][num_kv_heads][block_size][head_dim], row-major,
  *      separate tensors, same dtype.  Slot s = block * block_size + offset.
  *  - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
- *  - Supported: block_size 16, head_dim 64 or 128, dtype PKV_F32 or PKV_BF16
- *    (prefill: PKV_BF16 only), num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ *  - Supported: block_size 16 or 32 (the pages name both), head_dim 64 or 128,
+ *    dtype PKV_F32 or PKV_BF16 (cascade decode: PKV_BF16 only),
+ *    num_q_heads / num_kv_heads in {1, 2, 4, 8}.
  *    Anything else returns PKV_ERR_UNSUPPORTED before any launch.
  *  - Pointers marked "device" are CUDA device addresses owned by the caller; the
  *    library never frees or retains them after the call returns, and allocates no
@@ -58,7 +59,7 @@ typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 /* Description of one K pool and one V pool (same shape and dtype). */
 typedef struct pkv_pool_desc {
     int64_t num_blocks;   /* physical blocks in each pool */
-    int32_t block_size;   /* tokens per block (B); 16 */
+    int32_t block_size;   /* tokens per block (B); 16 or 32 */
     int32_t num_kv_heads; /* Hkv */
     int32_t head_dim;     /* D: 64 or 128 */
     int32_t dtype;        /* pkv_dtype */
@@ -163,7 +164,7 @@ pkv_status pkv_paged_decode_noalloc(const pkv_pool_desc* pool, void* out, const 
  *   prefix_len     > 0, a multiple of block_size; context_lens[s] >= prefix_len.
  *   max_context    host upper bound of context_lens (>= prefix_len).
  *   workspace      >= pkv_paged_decode_cascade_workspace_bytes(...) bytes, 16-byte aligned.
- * Other arguments as pkv_paged_decode.  Requires PKV_BF16 and head_dim 128. */
+ * Other arguments as pkv_paged_decode.  Requires PKV_BF16. */
 size_t pkv_paged_decode_cascade_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
                                                 int prefix_len, int max_context, int block_size,
                                                 int partition_blocks);
@@ -181,15 +182,16 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
  * That Does Not Forget"; aifetchly guide, "Prefill Bypass").  Request r has
  * cached_lens[r] tokens already in the pool followed by new_lens[r] new tokens whose
  * K/V must already be in the pool (kv_append first).  Query row q_offsets[r] + i
- * (i < new_lens[r]) attends keys 0 .. cached_lens[r] + i.  Runs on the tcgen05 tensor
- * cores with TMEM accumulators; bf16 in, fp32 accumulate, bf16 out.
- *   out, q        device [total_new][num_q_heads][head_dim] bf16.
+ * (i < new_lens[r]) attends keys 0 .. cached_lens[r] + i.  bf16 pools run on the
+ * tcgen05 tensor cores with TMEM accumulators (bf16 in, fp32 accumulate, bf16 out); fp32
+ * pools run each new token on the CUDA-core decode kernel (fp32 throughout).
+ *   out, q        device [total_new][num_q_heads][head_dim], the pools' dtype.
  *   block_tables  device int32 [num_reqs][max_blocks_per_seq].
  *   cached_lens, new_lens  device int32 [num_reqs]; cached >= 0, new >= 0,
  *                 cached + new <= max_blocks_per_seq * block_size.
  *   q_offsets     device int32 [num_reqs + 1], exclusive prefix sum of new_lens.
  *   max_new       host upper bound of new_lens (sizes the grid).
- * Requires PKV_BF16, head_dim 128, num_q_heads / num_kv_heads == 4. */
+ */
 pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q,
                              const void* k_pool, const void* v_pool,
                              const int32_t* block_tables, int max_blocks_per_seq,

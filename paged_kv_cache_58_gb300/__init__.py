@@ -199,15 +199,17 @@ def kv_append(k_pool, v_pool, slot_mapping, k, v, stream=None) -> None:
     _check("pkv_kv_append", st)
 
 
-def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context, partition_blocks=0):
+def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context, partition_blocks=0,
+                           block_size=BLOCK_SIZE):
     return int(_load().pkv_paged_decode_workspace_bytes(num_seqs, num_q_heads, head_dim,
-                                                        max_context, BLOCK_SIZE,
+                                                        max_context, block_size,
                                                         partition_blocks))
 
 
-def auto_partition(num_seqs, num_q_heads, max_context) -> int:
+def auto_partition(num_seqs, num_q_heads, max_context, block_size=BLOCK_SIZE) -> int:
+    """Partition size (in pool blocks) paged_decode picks when partition_blocks == 0."""
     return int(_load().pkv_paged_decode_auto_partition(num_seqs, num_q_heads, max_context,
-                                                       BLOCK_SIZE))
+                                                       block_size))
 
 
 def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *, max_context,
@@ -221,7 +223,7 @@ def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *, max_co
     S, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
-    need = decode_workspace_bytes(S, Hq, D, max_context, partition_blocks)
+    need = decode_workspace_bytes(S, Hq, D, max_context, partition_blocks, d.block_size)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wptr = workspace.data_ptr() if workspace is not None else None
@@ -239,21 +241,22 @@ def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *, max_co
 
 
 def cascade_workspace_bytes(num_seqs, num_q_heads, head_dim, prefix_len, max_context,
-                            partition_blocks=0):
+                            partition_blocks=0, block_size=BLOCK_SIZE):
     return int(_load().pkv_paged_decode_cascade_workspace_bytes(
-        num_seqs, num_q_heads, head_dim, prefix_len, max_context, BLOCK_SIZE, partition_blocks))
+        num_seqs, num_q_heads, head_dim, prefix_len, max_context, block_size, partition_blocks))
 
 
 def paged_decode_cascade(q, k_pool, v_pool, prefix_blocks, prefix_len, block_tables,
                          context_lens, scale, *, max_context, out=None, partition_blocks=0,
                          workspace=None, stream=None):
     """Decode of sequences sharing their first `prefix_len` tokens in `prefix_blocks`
-    (int32 [prefix_len / 16] CUDA tensor); same result as paged_decode."""
+    (int32 [prefix_len / block_size] CUDA tensor); same result as paged_decode."""
     d = pool_desc(k_pool)
     S, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
-    need = cascade_workspace_bytes(S, Hq, D, prefix_len, max_context, partition_blocks)
+    need = cascade_workspace_bytes(S, Hq, D, prefix_len, max_context, partition_blocks,
+                                   d.block_size)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     st = _load().pkv_paged_decode_cascade(

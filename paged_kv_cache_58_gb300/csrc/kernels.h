@@ -44,19 +44,30 @@ struct DecodeArgs {
     float* l_part;   // [S][Hq][max_parts]
     int* status;
     int64_t num_blocks;
-    int max_blocks_per_seq;
+    int max_blocks_per_seq;   // block-table row stride, in pool blocks
     int num_seqs;
     int num_q_heads;
     int num_kv_heads;
-    int partition_blocks;
-    int max_parts;     // partitions of the decoded block range per sequence
-    float scale_log2;  // softmax scale * log2(e)
-    // Cascade decode: blocks [0, block_offset) of every sequence were handled by a
+    // The kernels walk a sequence in 16-token chunks: chunk c is rows
+    // 16 (c & (2^chunk_shift - 1)) .. + 15 of the block in table entry c >> chunk_shift
+    // (chunk_shift = log2(block_size / 16): 0 for 16-token blocks, 1 for 32).
+    int chunk_shift;
+    int partition_chunks;   // 16-token chunks per split-KV partition
+    int max_parts;          // partitions of the decoded chunk range per sequence
+    float scale_log2;       // softmax scale * log2(e)
+    // Cascade decode: chunks [0, chunk_offset) of every sequence were handled by a
     // separate shared-prefix pass whose partial sits at partition 0; the split kernel
-    // covers blocks [block_offset, nblk) into partitions extra_parts.. and the combine
+    // covers chunks [chunk_offset, nchunks) into partitions extra_parts.. and the combine
     // merges extra_parts + max_parts partials per row.
-    int block_offset;
+    int chunk_offset;
     int extra_parts;
+    // Causal prefill on the CUDA-core kernel (fp32 pools): with cached_lens set the grid
+    // is (max_new, kv head, request) and CTA (i, kvh, r) decodes new token i of request
+    // r -- query row q_offsets[r] + i, keys 0 .. cached_lens[r] + i -- in one partition.
+    const int32_t* cached_lens;   // null: decode
+    const int32_t* new_lens;
+    const int32_t* q_offsets;
+    int max_new;
 };
 
 // CUDA-core decode (fp32 and bf16 pools): split kernel + combine.
@@ -90,6 +101,8 @@ cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs,
                                cudaStream_t stream);
 
 struct PrefillArgs {
+    int head_dim;     // 64 or 128
+    int block_size;   // tokens per pool block: 16 or 32
     void* out;
     const void* q;
     const void* k_pool;

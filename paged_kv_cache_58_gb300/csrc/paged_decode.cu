@@ -6,14 +6,14 @@
 // decode, aifetchly SGLang guide, "Integrating FlashInfer").  The arithmetic is
 // ordinary softmax attention; only the addressing is paged.
 //
-// Grid: (partition, kv head, sequence).  A CTA owns `partition_blocks` consecutive
-// logical blocks of one (sequence, kv head) and serves the G = Hq / Hkv query heads
-// that read that kv head, so each K/V byte is fetched from HBM once per step.
-// Inside the CTA each of the 4 warps streams every 4th block of the partition
-// through its own ring of shared-memory stages filled by 1-D bulk-async copies
-// (one 16-token K slab and one V slab per stage, both contiguous in the pool
-// layout), and keeps its own fp32 online-softmax state; the 4 states are merged
-// through shared memory at the end.
+// Grid: (partition, kv head, sequence).  A CTA owns `partition_chunks` consecutive
+// 16-token chunks of one (sequence, kv head) -- a chunk is a 16-token block, or half
+// of a 32-token one -- and serves the G = Hq / Hkv query heads that read that kv head,
+// so each K/V byte is fetched from HBM once per step.  Inside the CTA each of the 4
+// warps streams every 4th chunk of the partition through its own ring of
+// shared-memory stages filled by 1-D bulk-async copies (one 16-token K slab and one V
+// slab per stage, both contiguous in the pool layout), and keeps its own fp32
+// online-softmax state; the 4 states are merged through shared memory at the end.
 //
 // Lane mapping for one 16-token block: the two half-warps take alternate token
 // rows; lane c of a half-warp owns elements [c*NE, c*NE+NE) of D (NE = D/16).
@@ -141,24 +141,31 @@ decode_split_kernel(const DecodeArgs a) {
 
     griddep_wait();
     griddep_launch_dependents();
-    const int part = blockIdx.x;
     const int kvh = blockIdx.y;
-    const int seq = blockIdx.z;
+    // Decode: CTA (partition, kvh, sequence).  Prefill: CTA (token i, kvh, request r),
+    // one partition, table row r, query / output row q_offsets[r] + i.
+    const bool pre = a.cached_lens != nullptr;
+    const int part = pre ? 0 : static_cast<int>(blockIdx.x);
+    const int seq = blockIdx.z;   // table row
+    if (pre && static_cast<int>(blockIdx.x) >= a.new_lens[seq]) return;   // uniform
+    const size_t qrow = pre ? static_cast<size_t>(a.q_offsets[seq]) + blockIdx.x
+                            : static_cast<size_t>(seq);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int hw = lane >> 4;   // half-warp: token parity
     const int c = lane & 15;    // D slice
 
-    int L = a.context_lens[seq];
-    const int span_end = a.block_offset + a.max_parts * a.partition_blocks;  // blocks covered
-    if (L > a.max_blocks_per_seq * kBlock || L > span_end * kBlock) {
+    int L = pre ? a.cached_lens[seq] + static_cast<int>(blockIdx.x) + 1 : a.context_lens[seq];
+    const int span_end = a.chunk_offset + a.max_parts * a.partition_chunks;  // chunks covered
+    const int max_chunks = a.max_blocks_per_seq << a.chunk_shift;
+    if (L > max_chunks * kBlock || L > span_end * kBlock) {
         if (part == 0 && threadIdx.x == 0) raise_status(a.status, PKV_ERR_OOB);
-        L = min(a.max_blocks_per_seq, span_end) * kBlock;
+        L = min(max_chunks, span_end) * kBlock;
     }
     const int nblk = (L + kBlock - 1) / kBlock;
-    const int b0 = a.block_offset + part * a.partition_blocks;
+    const int b0 = a.chunk_offset + part * a.partition_chunks;
     if (L <= 0 || b0 >= nblk) return;  // uniform over the CTA, before any barrier
-    const int b1 = min(nblk, b0 + a.partition_blocks);
+    const int b1 = min(nblk, b0 + a.partition_chunks);
     const int my_first = b0 + warp;
     const int my_count = my_first < b1 ? (b1 - my_first + kWarps - 1) / kWarps : 0;
 
@@ -185,7 +192,7 @@ decode_split_kernel(const DecodeArgs a) {
     int ids = -1;
     auto fetch_ids = [&](int base) {
         const int i = base + lane;
-        ids = (i < my_count) ? __ldg(bt + my_first + i * kWarps) : -1;
+        ids = (i < my_count) ? __ldg(bt + ((my_first + i * kWarps) >> a.chunk_shift)) : -1;
     };
     fetch_ids(0);
 
@@ -197,7 +204,9 @@ decode_split_kernel(const DecodeArgs a) {
             mbar_arrive(bar);  // complete the phase without data; output is invalid
             return;
         }
-        const size_t off = (static_cast<size_t>(phys) * a.num_kv_heads + kvh) * kBlock * D;
+        const int ci = my_first + i * kWarps;   // chunk: rows 16 (ci & mask) of its block
+        const size_t off = (((static_cast<size_t>(phys) * a.num_kv_heads + kvh) << a.chunk_shift) +
+                            (ci & ((1 << a.chunk_shift) - 1))) * kBlock * D;
         mbar_arrive_expect_tx(bar, SM::kStageBytes);
         bulk_g2s(st, kpool + off, SM::kSlab, bar);
         bulk_g2s(st + SM::kSlab, vpool + off, SM::kSlab, bar);
@@ -216,7 +225,7 @@ decode_split_kernel(const DecodeArgs a) {
     float qf[G][NE];
     {
         const T* qbase = static_cast<const T*>(a.q) +
-                         (static_cast<size_t>(seq) * hq + kvh * G) * D + c * NE;
+                         (qrow * hq + kvh * G) * D + c * NE;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             load_chunk<T, NE>(qbase + g * D, qf[g]);
@@ -350,7 +359,7 @@ decode_split_kernel(const DecodeArgs a) {
             l = fmaf(f, ml[w * G + g], l);
         }
         const int h = kvh * G + g;
-        const size_t row = static_cast<size_t>(seq) * hq + h;
+        const size_t row = qrow * hq + h;
         if (nparts == 1) {
             store_elem<T>(static_cast<T*>(a.out) + row * D + d, o / l);
         } else {
@@ -382,12 +391,12 @@ decode_combine_kernel(const DecodeArgs a) {
     const size_t row = static_cast<size_t>(blockIdx.x) * kCombineWarps + warp;  // seq*Hq + h
     if (row >= static_cast<size_t>(a.num_seqs) * a.num_q_heads) return;
     const int seq = static_cast<int>(row / a.num_q_heads);
-    const int L = min(a.context_lens[seq], a.max_blocks_per_seq * kBlock);
+    const int L = min(a.context_lens[seq], (a.max_blocks_per_seq << a.chunk_shift) * kBlock);
     const int nblk = (L + kBlock - 1) / kBlock;
     const int total = a.max_parts + a.extra_parts;   // partial slots per row
     const int np = a.extra_parts +
-                   min(a.max_parts, max(0, (nblk - a.block_offset + a.partition_blocks - 1) /
-                                               a.partition_blocks));
+                   min(a.max_parts, max(0, (nblk - a.chunk_offset + a.partition_chunks - 1) /
+                                               a.partition_chunks));
     if (np <= 0) return;
     const float* mp = a.m_part + row * total;
     const float* lp = a.l_part + row * total;
@@ -448,7 +457,9 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
                                          SM::kTotal);
     if (e != cudaSuccess) return e;
     if (a.max_parts > 0) {   // zero when a cascade decode has no private suffix at all
-        dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
+        const unsigned gx = a.cached_lens ? static_cast<unsigned>(a.max_new)
+                                          : static_cast<unsigned>(a.max_parts);
+        dim3 grid(gx, a.num_kv_heads, a.num_seqs);
         e = launch_pdl(kern, grid, dim3(kThreads), SM::kTotal, stream, a);
         if (e != cudaSuccess) return e;
     }

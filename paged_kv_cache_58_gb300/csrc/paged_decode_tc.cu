@@ -108,15 +108,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int lane = threadIdx.x & 31;
 
     int L = a.context_lens[seq];
-    const int span_end = a.block_offset + a.max_parts * a.partition_blocks;  // blocks covered
-    if (L > a.max_blocks_per_seq * kBlk || L > span_end * kBlk) {
+    const int span_end = a.chunk_offset + a.max_parts * a.partition_chunks;  // chunks covered
+    const int max_chunks = a.max_blocks_per_seq << a.chunk_shift;
+    if (L > max_chunks * kBlk || L > span_end * kBlk) {
         if (part == 0 && threadIdx.x == 0) raise_status(a.status, PKV_ERR_OOB);
-        L = min(a.max_blocks_per_seq, span_end) * kBlk;
+        L = min(max_chunks, span_end) * kBlk;
     }
     const int nblk = (L + kBlk - 1) / kBlk;
-    const int b0 = a.block_offset + part * a.partition_blocks;
+    const int b0 = a.chunk_offset + part * a.partition_chunks;
     if (L <= 0 || b0 >= nblk) return;  // uniform over the CTA, before any barrier
-    const int b1 = min(nblk, b0 + a.partition_blocks);
+    const int b1 = min(nblk, b0 + a.partition_chunks);
     const int my_first = b0 + warp;
     const int my_count = my_first < b1 ? (b1 - my_first + kWarps - 1) / kWarps : 0;
 
@@ -137,7 +138,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     int ids = -1;
     auto fetch_ids = [&](int base) {
         const int i = base + lane;
-        ids = (i < my_count) ? __ldg(bt + my_first + i * kWarps) : -1;
+        ids = (i < my_count) ? __ldg(bt + ((my_first + i * kWarps) >> a.chunk_shift)) : -1;
     };
     fetch_ids(0);
 
@@ -149,7 +150,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const bool bad = phys < 0 || phys >= a.num_blocks;
         if (on && bad && lane == 0) raise_status(a.status, PKV_ERR_OOB);
         mbar_arrive_if(on && bad && lane == 0, bar);  // complete the phase without data
-        const int row = (bad ? kvh : phys * a.num_kv_heads + kvh) * kBlk;
+        const int ci = my_first + i * kWarps;   // chunk: rows 16 (ci & mask) of its block
+        const int row = ((bad ? kvh : phys * a.num_kv_heads + kvh) << a.chunk_shift) * kBlk +
+                        (ci & ((1 << a.chunk_shift) - 1)) * kBlk;
         mbar_arrive_expect_tx_if(on && !bad && lane == 0, bar, SM::kStageBytes);
         const bool mine = on && !bad && lane < 2;
         uint8_t* dst = st + (lane == 1 ? SM::kSlab : 0);
@@ -360,7 +363,7 @@ template <int D, int G>
 cudaError_t launch_tc(const DecodeArgs& a, cudaStream_t stream) {
     using SM = TcSmem<D, G>;
     CUtensorMap mk, mv;
-    const int64_t rows = a.num_blocks * a.num_kv_heads * kBlk;
+    const int64_t rows = a.num_blocks * a.num_kv_heads * (kBlk << a.chunk_shift);
     const bool maps_ok = D == 128 ? make_pool_block_map(&mk, a.k_pool, rows) &&
                                         make_pool_block_map(&mv, a.v_pool, rows)
                                   : make_pool_map(&mk, a.k_pool, rows, D) &&

@@ -70,20 +70,26 @@ namespace {
 
 constexpr int kRows = 128;                 // query rows per tile
 constexpr int kKeys = 128;                 // keys per KV tile
-constexpr int kHead = 128;                 // head_dim
-constexpr int kBlk = 16;                   // tokens per pool block
+constexpr int kChunk = 16;                 // tokens per staged chunk: a block, or half of one
 constexpr int kHalf = kRows * 128;         // one 64-column half of the 128-row Q tile: 16 KB
-constexpr int kTileBytes = 2 * kHalf;      // 32 KB
-constexpr int kBlockBytes = kBlk * 256;    // one pool block of one kv head: 16 rows x 256 B
-constexpr int kGroupBytes = 2048;          // K/V tiles: 8 rows x 2 halves x 128 B
 constexpr int kStagesK = 3;                // K stages: freed right after S = Q K^T
 constexpr int kStagesV = 3;                // V stages: freed after P.V
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
-constexpr int kOffV = kOffK + kStagesK * kTileBytes;
-constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
 constexpr int kNumBars = 21;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1 KB alignment slack
+
+// Shared-memory geometry for head_dim D (64 or 128).
+template <int D>
+struct Geom {
+    static constexpr int kHalves = D / 64;                // 64-column halves of a row
+    static constexpr int kQBytes = kRows * D * 2;         // Q tile
+    static constexpr int kTileBytes = kKeys * D * 2;      // one K or V stage
+    static constexpr int kChunkBytes = kChunk * D * 2;    // 16 rows of one kv head
+    static constexpr int kGroupBytes = 8 * D * 2;         // 8 key rows, every half
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kQBytes;
+    static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
+    static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
+    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
+};
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;                // issues stream 0 (even KV tiles); owns TMEM
@@ -126,11 +132,12 @@ PKV_DEVINL bool wait_bar_warp(const Ctl& c, int idx, uint32_t parity, int lane) 
     }
 }
 
-template <int G>
+template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+    using GM = Geom<D>;
     constexpr int TOK = kRows / G;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -150,7 +157,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int t0 = qt * TOK;
     if (t0 >= n) return;  // uniform over the CTA, before any barrier or TMEM use
     const int L = cascade ? c : c + n;       // keys in the pool for this request
-    if (c < 0 || L <= 0 || L > a.max_blocks_per_seq * kBlk) {
+    if (c < 0 || L <= 0 || L > a.max_blocks_per_seq * a.block_size) {
         if (threadIdx.x == 0) raise_status(a.status, PKV_ERR_OOB);
         return;
     }
@@ -163,8 +170,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int min_keys = cascade ? c : c + t0 + 1;
     const bool p_single = min_keys >= a.p_single_min_keys;   // uniform over the CTA
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GM::kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + GM::kOffBar + kNumBars * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     Ctl ctl{bars, abort_flag, a.status};
 
@@ -195,59 +202,75 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const uint32_t sQ = smem_u32(smem + kOffQ);
-    const uint32_t sK = smem_u32(smem + kOffK);
-    const uint32_t sV = smem_u32(smem + kOffV);
+    const uint32_t sQ = smem_u32(smem + GM::kOffQ);
+    const uint32_t sK = smem_u32(smem + GM::kOffK);
+    const uint32_t sV = smem_u32(smem + GM::kOffV);
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
-        // The whole warp runs the loop: each lane prefetches one block id (32 ids =
-        // 4 KV tiles per refill, independent loads), lane 0 sets the byte counts and
-        // lane b < 8 issues the box of block b of the tile.
+        // The whole warp runs the loop: each lane prefetches the block id of one 16-token
+        // chunk (32 chunks = 4 KV tiles per refill, independent loads), lane 0 sets the
+        // byte counts and lane b < 8 issues the box of chunk b of the tile.  A chunk is
+        // a whole block (block size 16) or rows 16 h .. 16 h + 15 of one (block size 32).
         const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
-        const int nblk_needed = max_lim / kBlk + 1;
+        const int nchunks = max_lim / kChunk + 1;
+        const int csh = a.block_size == 32 ? 1 : 0;   // log2 of chunks per block
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(&bars[BQ], kTileBytes);
-            tma_load_3d(smem + kOffQ, &tm_q, 0, kvh * G, qrow0, &bars[BQ]);
-            tma_load_3d(smem + kOffQ + kHalf, &tm_q, 64, kvh * G, qrow0, &bars[BQ]);
+            mbar_arrive_expect_tx(&bars[BQ], GM::kQBytes);
+#pragma unroll
+            for (int h = 0; h < GM::kHalves; ++h)
+                tma_load_3d(smem + GM::kOffQ + h * kHalf, &tm_q, 64 * h, kvh * G, qrow0,
+                            &bars[BQ]);
         }
         int ids = 0;
         int k_issued = 0, v_issued = 0;   // tiles whose K / V copies were issued
         for (int jt = 0; jt < ntiles; ++jt) {
-            constexpr int kPerTile = kKeys / kBlk;   // 8 blocks per KV tile
+            constexpr int kPerTile = kKeys / kChunk;   // 8 chunks per KV tile
             if ((jt & 3) == 0) {
                 const int i = jt * kPerTile + lane;
-                ids = (i < nblk_needed) ? __ldg(bt + i) : 0;
+                ids = (i < nchunks) ? __ldg(bt + (i >> csh)) : 0;
             }
             const int sk = jt % kStagesK;
             const int sv = jt % kStagesV;
-            const int nb = min(kPerTile, nblk_needed - jt * kPerTile);
+            const int nb = min(kPerTile, nchunks - jt * kPerTile);
             int phys = __shfl_sync(0xffffffffu, ids, ((jt & 3) * kPerTile) + (lane & 7));
             if (phys < 0 || phys >= a.num_blocks) {
                 if (lane < nb) raise_status(a.status, PKV_ERR_OOB);
                 phys = 0;  // keep the byte count; the output is flagged invalid
             }
-            const int row = (phys * a.num_kv_heads + kvh) * kBlk;
+            const int chunk = jt * kPerTile + (lane & 7);
+            const int row = (phys * a.num_kv_heads + kvh) * a.block_size +
+                            (chunk & ((1 << csh) - 1)) * kChunk;
             // K of tile jt: its stage is free once S of tile jt - kStagesK has run.  The
             // warp stays converged: lane 0 sets the byte count and lanes b < nb issue the
             // boxes through predicated instructions.
             if (jt >= kStagesK &&
                 !wait_bar_warp(ctl, BK_EMPTY + sk, ((jt / kStagesK) - 1) & 1, lane))
                 break;
-            mbar_arrive_expect_tx_if(lane == 0, &bars[BK_FULL + sk], nb * kBlockBytes);
-            tma_load_4d_if(lane < nb, smem + kOffK + sk * kTileBytes + lane * kBlockBytes, &tm_k,
-                           0, 0, 0, row / 8, &bars[BK_FULL + sk]);
+            mbar_arrive_expect_tx_if(lane == 0, &bars[BK_FULL + sk], nb * GM::kChunkBytes);
+            {
+                uint8_t* dst = smem + GM::kOffK + sk * GM::kTileBytes + lane * GM::kChunkBytes;
+                if constexpr (D == 128)
+                    tma_load_4d_if(lane < nb, dst, &tm_k, 0, 0, 0, row / 8, &bars[BK_FULL + sk]);
+                else
+                    tma_load_2d_if(lane < nb, dst, &tm_k, 0, row, &bars[BK_FULL + sk]);
+            }
             ++k_issued;
             // V of tile jt: its stage is free once P.V of tile jt - kStagesV has run.
             if (jt >= kStagesV &&
                 !wait_bar_warp(ctl, BV_EMPTY + sv, ((jt / kStagesV) - 1) & 1, lane))
                 break;
-            mbar_arrive_expect_tx_if(lane == 0, &bars[BV_FULL + sv], nb * kBlockBytes);
-            tma_load_4d_if(lane < nb, smem + kOffV + sv * kTileBytes + lane * kBlockBytes, &tm_v,
-                           0, 0, 0, row / 8, &bars[BV_FULL + sv]);
+            mbar_arrive_expect_tx_if(lane == 0, &bars[BV_FULL + sv], nb * GM::kChunkBytes);
+            {
+                uint8_t* dst = smem + GM::kOffV + sv * GM::kTileBytes + lane * GM::kChunkBytes;
+                if constexpr (D == 128)
+                    tma_load_4d_if(lane < nb, dst, &tm_v, 0, 0, 0, row / 8, &bars[BV_FULL + sv]);
+                else
+                    tma_load_2d_if(lane < nb, dst, &tm_v, 0, row, &bars[BV_FULL + sv]);
+            }
             ++v_issued;
         }
         // Drain (also after an abort): wait, bounded, until the last copy issued into
@@ -275,9 +298,9 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         // lanes poll, then one leader lane issues through predicated instructions), and
         // the descriptors are precomputed halves plus constant offsets.
         constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, kKeys, false, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, kHead, false, true);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, D, false, true);
         constexpr uint32_t hi_q = smem_desc_sw128_hi(1024);          // Q: 8-row atoms 1 KB apart
-        constexpr uint32_t hi_kv = smem_desc_sw128_hi(kGroupBytes);  // K/V: 8-key groups 2 KB apart
+        constexpr uint32_t hi_kv = smem_desc_sw128_hi(GM::kGroupBytes);  // K/V: 8-key groups
         const int sm = warp - kMmaWarp;
         const uint32_t lo_q = smem_desc_sw128_lo(sQ, 16);
         const uint32_t lo_k = smem_desc_sw128_lo(sK, 16);
@@ -294,9 +317,9 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (j >= 2 && !wait_bar_warp(ctl, BPV_DONE + sm, (use - 1) & 1, lane)) break;
             tc_fence_after();
             {
-                const uint32_t lk = lo_k + ((st * kTileBytes) >> 4);
+                const uint32_t lk = lo_k + ((st * GM::kTileBytes) >> 4);
 #pragma unroll
-                for (int ks = 0; ks < kHead / 16; ++ks) {
+                for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t kc = ((ks & 3) * 32) >> 4;   // 16 columns = 32 B
                     umma_bf16_if(leader, tS,
                                  desc_join(lo_q + (((ks >> 2) * kHalf) >> 4) + kc, hi_q),
@@ -311,11 +334,11 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (!wait_bar_warp(ctl, BV_FULL + st, (j / kStagesV) & 1, lane)) break;
             tc_fence_after();
             {
-                const uint32_t lv = lo_v + ((st * kTileBytes) >> 4);
+                const uint32_t lv = lo_v + ((st * GM::kTileBytes) >> 4);
                 // V as the MN-major B operand: 16 keys = two 8-key groups.
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks) {
-                    const uint64_t bv = desc_join(lv + ((ks * 2 * kGroupBytes) >> 4), hi_kv);
+                    const uint64_t bv = desc_join(lv + ((ks * 2 * GM::kGroupBytes) >> 4), hi_kv);
                     umma_bf16_ta_if(leader, tO, tS + ks * 8, bv, idesc_pv, (j >= 2) || (ks > 0));
                     if (!p_single) umma_bf16_ta_if(leader, tO, tS + 64 + ks * 8, bv, idesc_pv, true);
                 }
@@ -384,7 +407,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < D / 32; ++q) {
                     float o[32];
                     const uint32_t ta = tmem + lane_addr + kTmemO + sm * 128 + q * 32;
                     tmem_ld32(ta, o);
@@ -463,14 +486,14 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                     break;
                 }
                 if (kbase + row > max_lim) {
-                    uint8_t* vrow = smem + kOffV + (jt % kStagesV) * kTileBytes +
-                                    (row >> 3) * kGroupBytes + (row & 7) * 128;
+                    uint8_t* vrow = smem + GM::kOffV + (jt % kStagesV) * GM::kTileBytes +
+                                    (row >> 3) * GM::kGroupBytes + (row & 7) * 128;
                     const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        *reinterpret_cast<uint4*>(vrow + (j << 4)) = z;
-                        *reinterpret_cast<uint4*>(vrow + 1024 + (j << 4)) = z;
-                    }
+                    for (int h = 0; h < GM::kHalves; ++h)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<uint4*>(vrow + h * 1024 + (j << 4)) = z;
                 }
                 fence_proxy_async_smem();
             }
@@ -493,14 +516,14 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             const float lsum = a0 * l_st[0] + a1 * l_st[1];
             const float c0 = a0 / lsum, c1 = a1 / lsum;
             const size_t orow_idx = static_cast<size_t>(qoff + tok) * a.num_q_heads + head;
-            uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * kHead;
+            uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * D;
             const size_t prow = orow_idx * a.max_parts_total;   // cascade: partition 0
             if (cascade && row_valid) {
                 a.m_part[prow] = m;   // log2 domain, as the decode partials
                 a.l_part[prow] = lsum;
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < D / 32; ++q) {
                 float o[32];
                 tmem_ld32(tmem + lane_addr + kTmemO + q * 32, o);
                 tmem_wait_ld();
@@ -514,7 +537,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                     for (int e = 0; e < 32; ++e) o[e] = fmaf(o1[e], c1, o[e]);
                 }
                 if (cascade && row_valid) {
-                    float* dst = a.o_part + prow * kHead + q * 32;
+                    float* dst = a.o_part + prow * D + q * 32;
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
                         *reinterpret_cast<float4*>(dst + e) =
@@ -543,32 +566,44 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
 }
 
-template <int G>
+template <int D, int G>
 cudaError_t launch_g(const PrefillArgs& a, cudaStream_t stream) {
+    using GM = Geom<D>;
     CUtensorMap mq, mk, mv;
-    const int64_t rows = a.num_blocks * a.num_kv_heads * kBlk;
-    if (!make_q_group_map(&mq, a.q, a.total_new, a.num_q_heads, kHead, G, kRows / G) ||
-        !make_pool_block_map(&mk, a.k_pool, rows) || !make_pool_block_map(&mv, a.v_pool, rows))
+    const int64_t rows = a.num_blocks * a.num_kv_heads * a.block_size;
+    const bool pool_ok = D == 128 ? make_pool_block_map(&mk, a.k_pool, rows) &&
+                                        make_pool_block_map(&mv, a.v_pool, rows)
+                                  : make_pool_map(&mk, a.k_pool, rows, D) &&
+                                        make_pool_map(&mv, a.v_pool, rows, D);
+    if (!pool_ok || !make_q_group_map(&mq, a.q, a.total_new, a.num_q_heads, D, G, kRows / G))
         return cudaErrorInvalidValue;
-    auto kern = prefill_tcgen05_kernel<G>;
+    auto kern = prefill_tcgen05_kernel<D, G>;
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GM::kSmemBytes);
     if (e != cudaSuccess) return e;
     constexpr int TOK = kRows / G;
     dim3 grid((a.max_new + TOK - 1) / TOK, a.num_kv_heads, a.num_reqs);
-    return launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, stream, mq, mk, mv, a);
+    return launch_pdl(kern, grid, dim3(kThreads), GM::kSmemBytes, stream, mq, mk, mv, a);
+}
+
+template <int D>
+cudaError_t launch_d(const PrefillArgs& a, int group, cudaStream_t stream) {
+    switch (group) {
+        case 1: return launch_g<D, 1>(a, stream);
+        case 2: return launch_g<D, 2>(a, stream);
+        case 4: return launch_g<D, 4>(a, stream);
+        case 8: return launch_g<D, 8>(a, stream);
+        default: return cudaErrorNotSupported;
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_paged_prefill(const PrefillArgs& a, int group, cudaStream_t stream) {
-    switch (group) {
-        case 1: return launch_g<1>(a, stream);
-        case 2: return launch_g<2>(a, stream);
-        case 4: return launch_g<4>(a, stream);
-        case 8: return launch_g<8>(a, stream);
-        default: return cudaErrorNotSupported;
-    }
+    if (a.block_size != 16 && a.block_size != 32) return cudaErrorNotSupported;
+    if (a.head_dim == 128) return launch_d<128>(a, group, stream);
+    if (a.head_dim == 64) return launch_d<64>(a, group, stream);
+    return cudaErrorNotSupported;
 }
 
 }  // namespace pkv

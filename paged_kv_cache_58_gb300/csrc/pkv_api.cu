@@ -13,7 +13,10 @@
 
 namespace {
 
-constexpr int kBlockSize = 16;
+constexpr int kChunk = 16;   // the kernels walk sequences in 16-token chunks
+
+// log2(block_size / 16) for the supported block sizes 16 and 32, else -1.
+int chunk_shift(int block_size) { return block_size == 16 ? 0 : block_size == 32 ? 1 : -1; }
 constexpr int kMaxDevices = 64;
 constexpr double kLog2e = 1.4426950408889634;
 
@@ -47,7 +50,7 @@ pkv_status check_pool(const pkv_pool_desc* pool) {
         pool->block_size <= 0)
         return PKV_ERR_INVALID;
     if (pool->dtype != PKV_F32 && pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-    if (pool->block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+    if (chunk_shift(pool->block_size) < 0) return PKV_ERR_UNSUPPORTED;
     if (pool->head_dim != 64 && pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (pool->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
     if (pool->num_blocks > INT32_MAX) return PKV_ERR_UNSUPPORTED;
@@ -58,25 +61,31 @@ pkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
-// Partition policy for split-KV decode: at least 64 blocks (1024 tokens) per
-// partition -- each CTA pays a fixed start-up (block ids, first copies in flight,
-// merge), and on the Llama-3-8B-shaped batch 64 blocks measured best (16: 81 %,
-// 32: 89 %, 64: 90 % of the copy bandwidth) -- and at most 64 partitions per
-// sequence to bound the workspace; shrink partitions (down to 8 blocks) while
-// fewer than 2 x 152 CTAs would be busy.
+// Partition policy for split-KV decode, in 16-token chunks: at least 64 chunks (1024
+// tokens) per partition -- each CTA pays a fixed start-up (block ids, first copies
+// in flight, merge), and on the Llama-3-8B-shaped batch 64 chunks measured best (16:
+// 81 %, 32: 89 %, 64: 90 % of the copy bandwidth) -- and at most 64 partitions per
+// sequence to bound the workspace; shrink partitions (down to 8 chunks) while fewer
+// than 2 x 152 CTAs would be busy.  The result is a multiple of 4 chunks (one per warp
+// per step) and of 2 (a whole number of 32-token blocks).
 // The CTA estimate counts ceil(Hq / 8) kv heads per sequence (a lower bound: a
 // GQA group is at most 8 query heads) so that the choice, and with it the
 // workspace size, depends only on (num_seqs, num_q_heads, max_context).
-int auto_partition(int num_seqs, int num_q_heads, int max_context) {
-    const int max_blocks = ceil_div(max_context, kBlockSize);
+int auto_partition_chunks(int num_seqs, int num_q_heads, int max_context) {
+    const int max_chunks = ceil_div(max_context, kChunk);
     const int64_t kv_heads_min = ceil_div(num_q_heads, 8);
-    int pb = ceil_div(max_blocks, 64);
-    if (pb < 64) pb = 64;
-    pb = (pb + 3) / 4 * 4;
-    while (pb > 8 && static_cast<int64_t>(num_seqs) * kv_heads_min * ceil_div(max_blocks, pb) <
+    int pc = ceil_div(max_chunks, 64);
+    if (pc < 64) pc = 64;
+    pc = (pc + 3) / 4 * 4;
+    while (pc > 8 && static_cast<int64_t>(num_seqs) * kv_heads_min * ceil_div(max_chunks, pc) <
                          304)
-        pb /= 2;
-    return pb;
+        pc /= 2;
+    return pc;
+}
+
+// The same in pool blocks.
+int auto_partition(int num_seqs, int num_q_heads, int max_context, int block_size) {
+    return auto_partition_chunks(num_seqs, num_q_heads, max_context) >> chunk_shift(block_size);
 }
 
 // bf16 decode runs on the tensor-core kernel; PKV_DECODE_KERNEL=simt selects the
@@ -177,18 +186,19 @@ pkv_status pkv_kv_append(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
 
 int pkv_paged_decode_auto_partition(int num_seqs, int num_q_heads, int max_context,
                                     int block_size) {
-    if (num_seqs <= 0 || num_q_heads <= 0 || max_context <= 0 || block_size != kBlockSize)
+    if (num_seqs <= 0 || num_q_heads <= 0 || max_context <= 0 || chunk_shift(block_size) < 0)
         return 0;
-    return auto_partition(num_seqs, num_q_heads, max_context);
+    return auto_partition(num_seqs, num_q_heads, max_context, block_size);
 }
 
 size_t pkv_paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
                                         int max_context, int block_size, int partition_blocks) {
     if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context <= 0 ||
-        block_size != kBlockSize || partition_blocks < 0)
+        chunk_shift(block_size) < 0 || partition_blocks < 0)
         return 0;
-    const int pb = partition_blocks ? partition_blocks : auto_partition(num_seqs, num_q_heads, max_context);
-    const int max_parts = ceil_div(ceil_div(max_context, kBlockSize), pb);
+    const int pb = partition_blocks ? partition_blocks
+                                    : auto_partition(num_seqs, num_q_heads, max_context, block_size);
+    const int max_parts = ceil_div(ceil_div(max_context, block_size), pb);
     return decode_workspace(num_seqs, num_q_heads, head_dim, max_parts);
 }
 
@@ -204,8 +214,9 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
     if (num_seqs == 0) return PKV_OK;
     if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens)
         return PKV_ERR_INVALID;
+    const int B = pool->block_size;
     if (max_blocks_per_seq <= 0 || max_context <= 0 ||
-        static_cast<int64_t>(max_context) > static_cast<int64_t>(max_blocks_per_seq) * kBlockSize)
+        static_cast<int64_t>(max_context) > static_cast<int64_t>(max_blocks_per_seq) * B)
         return PKV_ERR_INVALID;
     if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID;
     const int group = num_q_heads / pool->num_kv_heads;
@@ -214,8 +225,9 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return PKV_ERR_INVALID;
 
-    const int pb = partition_blocks ? partition_blocks : auto_partition(num_seqs, num_q_heads, max_context);
-    const int max_parts = ceil_div(ceil_div(max_context, kBlockSize), pb);
+    const int pb = partition_blocks ? partition_blocks
+                                    : auto_partition(num_seqs, num_q_heads, max_context, B);
+    const int max_parts = ceil_div(ceil_div(max_context, B), pb);
     if (max_parts > pkv::kMaxParts) return PKV_ERR_UNSUPPORTED;
     const size_t need = decode_workspace(num_seqs, num_q_heads, pool->head_dim, max_parts);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
@@ -236,7 +248,8 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
     a.num_seqs = num_seqs;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = pool->num_kv_heads;
-    a.partition_blocks = pb;
+    a.chunk_shift = chunk_shift(B);
+    a.partition_chunks = pb << a.chunk_shift;
     a.max_parts = max_parts;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     if (need > 0) {
@@ -281,12 +294,13 @@ size_t pkv_paged_decode_cascade_workspace_bytes(int num_seqs, int num_q_heads, i
                                                 int prefix_len, int max_context, int block_size,
                                                 int partition_blocks) {
     if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || prefix_len <= 0 ||
-        max_context < prefix_len || block_size != kBlockSize || partition_blocks < 0)
+        max_context < prefix_len || chunk_shift(block_size) < 0 || partition_blocks < 0)
         return 0;
     const int suffix = max_context - prefix_len;
-    const int pb = partition_blocks ? partition_blocks
-                                    : (suffix > 0 ? auto_partition(num_seqs, num_q_heads, suffix) : 1);
-    const int parts = suffix > 0 ? ceil_div(ceil_div(suffix, kBlockSize), pb) : 0;
+    const int pb = partition_blocks
+                       ? partition_blocks
+                       : (suffix > 0 ? auto_partition(num_seqs, num_q_heads, suffix, block_size) : 1);
+    const int parts = suffix > 0 ? ceil_div(ceil_div(suffix, block_size), pb) : 0;
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * (parts + 1);
     const size_t ml = (rows * sizeof(float) + 15) / 16 * 16;
     return rows * head_dim * sizeof(float) + 2 * ml;
@@ -306,25 +320,26 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
     if (num_seqs == 0) return PKV_OK;
     if (!out || !q || !k_pool || !v_pool || !prefix_blocks || !block_tables || !context_lens)
         return PKV_ERR_INVALID;
-    if (prefix_len <= 0 || prefix_len % kBlockSize != 0 || max_context < prefix_len ||
+    const int B = pool->block_size;
+    if (prefix_len <= 0 || prefix_len % B != 0 || max_context < prefix_len ||
         max_blocks_per_seq <= 0 ||
-        static_cast<int64_t>(max_context) > static_cast<int64_t>(max_blocks_per_seq) * kBlockSize)
+        static_cast<int64_t>(max_context) > static_cast<int64_t>(max_blocks_per_seq) * B)
         return PKV_ERR_INVALID;
     if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID;
     const int group = num_q_heads / pool->num_kv_heads;
-    if (pool->dtype != PKV_BF16 || pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
     if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_ERR_UNSUPPORTED;
     if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return PKV_ERR_INVALID;
     const int suffix = max_context - prefix_len;
-    const int pb = partition_blocks ? partition_blocks
-                                    : (suffix > 0 ? auto_partition(num_seqs, num_q_heads, suffix) : 1);
-    const int parts = suffix > 0 ? ceil_div(ceil_div(suffix, kBlockSize), pb) : 0;
+    const int pb = partition_blocks
+                       ? partition_blocks
+                       : (suffix > 0 ? auto_partition(num_seqs, num_q_heads, suffix, B) : 1);
+    const int parts = suffix > 0 ? ceil_div(ceil_div(suffix, B), pb) : 0;
     if (parts + 1 > pkv::kMaxParts) return PKV_ERR_UNSUPPORTED;
     const size_t need = pkv_paged_decode_cascade_workspace_bytes(
-        num_seqs, num_q_heads, pool->head_dim, prefix_len, max_context, kBlockSize,
-        partition_blocks);
+        num_seqs, num_q_heads, pool->head_dim, prefix_len, max_context, B, partition_blocks);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_NOMEM;
     int* status = status_word();
     if (!status) return PKV_ERR_CUDA;
@@ -339,13 +354,15 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
 
     // 1. every sequence's query heads against the shared prefix, on the tensor cores
     pkv::PrefillArgs pa{};
+    pa.head_dim = pool->head_dim;
+    pa.block_size = B;
     pa.q = q;
     pa.k_pool = k_pool;
     pa.v_pool = v_pool;
     pa.block_tables = prefix_blocks;
     pa.status = status;
     pa.num_blocks = pool->num_blocks;
-    pa.max_blocks_per_seq = prefix_len / kBlockSize;
+    pa.max_blocks_per_seq = prefix_len / B;
     pa.num_reqs = 1;
     pa.total_new = num_seqs;
     pa.max_new = num_seqs;
@@ -377,13 +394,14 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
     a.num_seqs = num_seqs;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = pool->num_kv_heads;
-    a.partition_blocks = pb;
+    a.chunk_shift = chunk_shift(B);
+    a.partition_chunks = pb << a.chunk_shift;
     a.max_parts = parts;
     a.scale_log2 = sl2;
     a.o_part = o_part;
     a.m_part = m_part;
     a.l_part = l_part;
-    a.block_offset = prefix_len / kBlockSize;
+    a.chunk_offset = prefix_len / kChunk;
     a.extra_parts = 1;
     if (decode_use_simt())
         return from_cuda(pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_));
@@ -406,14 +424,41 @@ pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q
         return PKV_ERR_INVALID;
     if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID;
     const int group = num_q_heads / pool->num_kv_heads;
-    if (pool->dtype != PKV_BF16 || pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_ERR_UNSUPPORTED;
     if (num_reqs > 65535) return PKV_ERR_UNSUPPORTED;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return PKV_ERR_INVALID;
     int* status = status_word();
     if (!status) return PKV_ERR_CUDA;
+    if (pool->dtype == PKV_F32) {
+        // fp32 pools: each new token decoded on the CUDA-core kernel over keys 0 .. c + i
+        // (no tensor cores: fp32 operands would have to be rounded to tf32).
+        pkv::DecodeArgs d{};
+        d.out = out;
+        d.q = q;
+        d.k_pool = k_pool;
+        d.v_pool = v_pool;
+        d.block_tables = block_tables;
+        d.status = status;
+        d.num_blocks = pool->num_blocks;
+        d.max_blocks_per_seq = max_blocks_per_seq;
+        d.num_seqs = num_reqs;
+        d.num_q_heads = num_q_heads;
+        d.num_kv_heads = pool->num_kv_heads;
+        d.chunk_shift = chunk_shift(pool->block_size);
+        d.partition_chunks = max_blocks_per_seq << d.chunk_shift;   // one partition
+        d.max_parts = 1;
+        d.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+        d.cached_lens = cached_lens;
+        d.new_lens = new_lens;
+        d.q_offsets = q_offsets;
+        d.max_new = max_new;
+        return from_cuda(pkv::launch_paged_decode(d, pool->dtype, pool->head_dim, group,
+                                                  static_cast<cudaStream_t>(stream)));
+    }
     pkv::PrefillArgs a{};
+    a.head_dim = pool->head_dim;
+    a.block_size = pool->block_size;
     a.out = out;
     a.q = q;
     a.k_pool = k_pool;

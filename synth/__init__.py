@@ -49,6 +49,7 @@ class Workload:
     ctx_hi: int = 0
     shared_prefix: int = 0    # tokens of a prefix shared by all sequences (multiple of B)
     new_tokens: int = 0       # prefill: new tokens per request
+    block_size: int = BLOCK   # tokens per pool block (16, or 32)
 
 
 WORKLOADS = {
@@ -131,7 +132,7 @@ def build_case(wl: Workload | str, device="cuda", *, lengths=None, seed=None,
     g_dev = _gen(seed + 1000, device)
     lens = list(lengths) if lengths is not None else draw_lengths(wl, g_cpu)
     S, Hq, Hkv, D = len(lens), wl.num_q_heads, wl.num_kv_heads, wl.head_dim
-    B = BLOCK
+    B = wl.block_size
 
     if wl.kind == "decode":
         if wl.shared_prefix:

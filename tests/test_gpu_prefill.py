@@ -31,10 +31,11 @@ def run_prefill(pkv, case):
     return out
 
 
-def custom_case(hq, hkv, cached, new, seed, num_blocks=1024):
-    """Prefill case with per-request new lengths (the workload recipe fixes n)."""
+def custom_case(hq, hkv, cached, new, seed, num_blocks=1024, **over):
+    """Prefill case with per-request new lengths (the workload recipe fixes n); `over`
+    replaces further recipe fields (head_dim, block_size)."""
     wl = dataclasses.replace(synth.WORKLOADS["prefill"], num_q_heads=hq, num_kv_heads=hkv,
-                             new_tokens=max(new), num_blocks=num_blocks)
+                             new_tokens=max(new), num_blocks=num_blocks, **over)
     case = synth.build_case(wl, "cuda", lengths=cached, seed=seed)
     if all(x == max(new) for x in new):
         return case

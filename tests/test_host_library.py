@@ -71,12 +71,13 @@ def test_sixty_token_response_takes_four_blocks(pkv):
 
 
 def _invariants(a, seqs):
+    B = a.block_size
     held = {}
     used = set()
     for sid in seqs:
         n = a.seq_num_blocks(sid)
         L = a.seq_len(sid)
-        assert 0 <= n * 16 - L < 16 or (L == 0 and n == 0), (sid, n, L)
+        assert 0 <= n * B - L < B or (L == 0 and n == 0), (sid, n, L)
         row = a.block_table([sid], max(n, 1))[0].tolist()
         for b in row[:n]:
             held[b] = held.get(b, 0) + 1
@@ -86,11 +87,12 @@ def _invariants(a, seqs):
     assert a.num_free + len(used) == a.num_blocks
 
 
-def test_random_workload_waste_bound_and_conservation(pkv):
+@pytest.mark.parametrize("block_size", [16, 32])
+def test_random_workload_waste_bound_and_conservation(pkv, block_size):
     g = json.load(open(GOLDEN))["waste_bound"]
     assert g["max_partial_blocks_per_sequence"] == 1
     rng = np.random.default_rng(0)
-    a = pkv.BlockAllocator(4000, seed=3)
+    a = pkv.BlockAllocator(4000, block_size=block_size, seed=3)
     live = []
     nxt = 0
     for step in range(600):
@@ -197,3 +199,9 @@ def test_decode_workspace_and_partition_policy(pkv):
     assert pb == 128 and -(-8192 // pb) == 64
     # a single short sequence needs no workspace
     assert pkv.decode_workspace_bytes(1, 8, 128, 64) == 0
+    # 32-token blocks: the same 1024-token partitions (32 blocks), the same workspace
+    assert pkv.auto_partition(64, 32, 4096, block_size=32) == 32
+    assert pkv.decode_workspace_bytes(64, 32, 128, 4096, block_size=32) == ws
+    assert pkv.auto_partition(16, 64, 131072, block_size=32) == 64
+    # other block sizes are not supported
+    assert pkv.auto_partition(64, 32, 4096, block_size=8) == 0
