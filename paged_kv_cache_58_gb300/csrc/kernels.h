@@ -61,6 +61,7 @@ struct DecodeArgs {
     // merges extra_parts + max_parts partials per row.
     int chunk_offset;
     int extra_parts;
+    int defer_combine;   // nonzero: the launcher leaves the combine to the caller
     // Causal prefill on the CUDA-core kernel (fp32 pools): with cached_lens set the grid
     // is (max_new, kv head, request) and CTA (i, kvh, r) decodes new token i of request
     // r -- query row q_offsets[r] + i, keys 0 .. cached_lens[r] + i -- in one partition.
@@ -120,13 +121,15 @@ struct PrefillArgs {
     int num_q_heads;
     int num_kv_heads;
     float scale_log2;
-    // Cascade mode (shared-prefix decode): one "request" whose cached_lens[0] keys are
-    // the shared prefix and whose new_lens[0] query rows are the sequences (one token
-    // each); every row attends all prefix keys (no causal mask) and the result goes to
-    // the split-KV partials (partition 0 of max_parts_total) instead of `out`.
+    // Cascade mode (shared-prefix decode): one "request" whose cascade_keys keys are the
+    // shared prefix and whose cascade_rows query rows are the sequences (one token each);
+    // every row attends all prefix keys (no causal mask), the grid's z dimension splits
+    // the prefix's tiles (cascade_tiles_per_split each) and split z writes its partial to
+    // slot z of the split-KV partials (max_parts_total slots per row) instead of `out`.
     int cascade;
     int cascade_keys;   // cascade: prefix length (keys); rows come from cascade_rows
     int cascade_rows;   // cascade: number of sequences (query rows per head)
+    int cascade_tiles_per_split;   // cascade: 128-key tiles per split (grid z = splits)
     int max_parts_total;
     float* o_part;
     float* m_part;

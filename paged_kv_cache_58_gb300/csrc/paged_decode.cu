@@ -464,6 +464,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     if (a.extra_parts == 0 && a.max_parts == 1) return e;  // output written directly
+    if (a.defer_combine) return e;
     return launch_decode_combine(a, sizeof(T) == 2 ? PKV_BF16 : PKV_F32, D, stream);
 }
 

@@ -379,6 +379,7 @@ cudaError_t launch_tc(const DecodeArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     if (a.extra_parts == 0 && a.max_parts == 1) return e;  // output written directly
+    if (a.defer_combine) return e;
     return launch_decode_combine(a, PKV_BF16, D, stream);
 }
 

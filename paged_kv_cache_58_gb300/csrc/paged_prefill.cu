@@ -163,7 +163,13 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     const int i_last = min(t0 + TOK, n) - 1;
     const int max_lim = cascade ? c - 1 : c + i_last;   // last key any row of this tile sees
-    const int ntiles = max_lim / kKeys + 1;
+    // KV tiles [j0, j0 + ntiles) of this CTA: all of them, or in cascade mode the range
+    // of split blockIdx.z (its partial goes to slot blockIdx.z; the host sizes the
+    // splits so that none is empty).
+    const int j0 = cascade ? r * a.cascade_tiles_per_split : 0;
+    const int ntiles =
+        cascade ? min(max_lim / kKeys + 1 - j0, a.cascade_tiles_per_split) : max_lim / kKeys + 1;
+    if (ntiles <= 0) return;   // uniform over the CTA, before any barrier or TMEM use
     const int qoff = cascade ? 0 : a.q_offsets[r];
     const int qrow0 = qoff + t0;             // first token row of the tile in q / out
     // Every row of the tile attends at least min_keys keys (its first token the fewest).
@@ -212,7 +218,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         // chunk (32 chunks = 4 KV tiles per refill, independent loads), lane 0 sets the
         // byte counts and lane b < 8 issues the box of chunk b of the tile.  A chunk is
         // a whole block (block size 16) or rows 16 h .. 16 h + 15 of one (block size 32).
-        const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
+        const int32_t* bt =
+            a.block_tables + static_cast<size_t>(cascade ? 0 : r) * a.max_blocks_per_seq;
         const int nchunks = max_lim / kChunk + 1;
         const int csh = a.block_size == 32 ? 1 : 0;   // log2 of chunks per block
         if (lane == 0) {
@@ -230,18 +237,18 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int jt = 0; jt < ntiles; ++jt) {
             constexpr int kPerTile = kKeys / kChunk;   // 8 chunks per KV tile
             if ((jt & 3) == 0) {
-                const int i = jt * kPerTile + lane;
+                const int i = (j0 + jt) * kPerTile + lane;
                 ids = (i < nchunks) ? __ldg(bt + (i >> csh)) : 0;
             }
             const int sk = jt % kStagesK;
             const int sv = jt % kStagesV;
-            const int nb = min(kPerTile, nchunks - jt * kPerTile);
+            const int nb = min(kPerTile, nchunks - (j0 + jt) * kPerTile);
             int phys = __shfl_sync(0xffffffffu, ids, ((jt & 3) * kPerTile) + (lane & 7));
             if (phys < 0 || phys >= a.num_blocks) {
                 if (lane < nb) raise_status(a.status, PKV_ERR_OOB);
                 phys = 0;  // keep the byte count; the output is flagged invalid
             }
-            const int chunk = jt * kPerTile + (lane & 7);
+            const int chunk = (j0 + jt) * kPerTile + (lane & 7);
             const int row = (phys * a.num_kv_heads + kvh) * a.block_size +
                             (chunk & ((1 << csh) - 1)) * kChunk;
             // K of tile jt: its stage is free once S of tile jt - kStagesK has run.  The
@@ -375,7 +382,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tmem_ld32(tS + q * 32, *reinterpret_cast<float(*)[32]>(&x[q * 32]));
             tmem_wait_ld();
 
-            const int kbase = jt * kKeys;
+            const int kbase = (j0 + jt) * kKeys;
             if (kbase + kKeys - 1 > lim) {
 #pragma unroll
                 for (int k = 0; k < kKeys; ++k) x[k] = (kbase + k <= lim) ? x[k] : -INFINITY;
@@ -517,7 +524,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             const float c0 = a0 / lsum, c1 = a1 / lsum;
             const size_t orow_idx = static_cast<size_t>(qoff + tok) * a.num_q_heads + head;
             uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * D;
-            const size_t prow = orow_idx * a.max_parts_total;   // cascade: partition 0
+            const size_t prow = orow_idx * a.max_parts_total + r;   // cascade: slot = split
             if (cascade && row_valid) {
                 a.m_part[prow] = m;   // log2 domain, as the decode partials
                 a.l_part[prow] = lsum;

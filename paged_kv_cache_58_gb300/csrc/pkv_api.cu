@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <algorithm>
 #include <climits>
 #include <cstring>
 #include <mutex>
@@ -38,6 +39,21 @@ int* status_word() {
         g_status_addr[dev] = static_cast<int*>(p);
     }
     return g_status_addr[dev];
+}
+
+std::mutex g_side_mu;
+cudaStream_t g_side_stream[kMaxDevices] = {nullptr};
+
+// A library-owned non-blocking stream per device, for work that runs beside the
+// caller's stream inside one call (joined back before the call's last launch).
+cudaStream_t side_stream() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_side_mu);
+    if (!g_side_stream[dev] &&
+        cudaStreamCreateWithFlags(&g_side_stream[dev], cudaStreamNonBlocking) != cudaSuccess)
+        g_side_stream[dev] = nullptr;
+    return g_side_stream[dev];
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -290,6 +306,25 @@ pkv_status pkv_paged_decode_noalloc(const pkv_pool_desc* pool, void* out, const 
                             partition_blocks, scratch, need, stream);
 }
 
+namespace {
+
+// Splits of the cascade decode's prefix pass over its 128-key tiles.  The pass has about
+// ceil(S * Hq / 128) CTAs (query tiles times kv heads) and runs beside the suffix
+// decode, which is HBM-bound; when it would have fewer than half the SMs its tiles are
+// divided among up to 8 CTAs per query tile (none empty), each writing its own partial
+// slot.  Depends only on (num_seqs, num_q_heads, prefix_len).
+int cascade_splits(int num_seqs, int num_q_heads, int prefix_len, int* tiles_per_split) {
+    const int tiles = ceil_div(prefix_len, 128);
+    const int ctas = ceil_div(static_cast<int64_t>(num_seqs) * num_q_heads, 128);
+    int ns = ceil_div(76, ctas);
+    ns = std::max(1, std::min(ns, std::min(8, tiles)));
+    const int tps = ceil_div(tiles, ns);
+    *tiles_per_split = tps;
+    return ceil_div(tiles, tps);
+}
+
+}  // namespace
+
 size_t pkv_paged_decode_cascade_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
                                                 int prefix_len, int max_context, int block_size,
                                                 int partition_blocks) {
@@ -301,7 +336,9 @@ size_t pkv_paged_decode_cascade_workspace_bytes(int num_seqs, int num_q_heads, i
                        ? partition_blocks
                        : (suffix > 0 ? auto_partition(num_seqs, num_q_heads, suffix, block_size) : 1);
     const int parts = suffix > 0 ? ceil_div(ceil_div(suffix, block_size), pb) : 0;
-    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * (parts + 1);
+    int tps = 0;
+    const int ns = cascade_splits(num_seqs, num_q_heads, prefix_len, &tps);
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * (parts + ns);
     const size_t ml = (rows * sizeof(float) + 15) / 16 * 16;
     return rows * head_dim * sizeof(float) + 2 * ml;
 }
@@ -337,13 +374,15 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
                        ? partition_blocks
                        : (suffix > 0 ? auto_partition(num_seqs, num_q_heads, suffix, B) : 1);
     const int parts = suffix > 0 ? ceil_div(ceil_div(suffix, B), pb) : 0;
-    if (parts + 1 > pkv::kMaxParts) return PKV_ERR_UNSUPPORTED;
+    int tps = 0;
+    const int ns = cascade_splits(num_seqs, num_q_heads, prefix_len, &tps);
+    if (parts + ns > pkv::kMaxParts) return PKV_ERR_UNSUPPORTED;
     const size_t need = pkv_paged_decode_cascade_workspace_bytes(
         num_seqs, num_q_heads, pool->head_dim, prefix_len, max_context, B, partition_blocks);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_NOMEM;
     int* status = status_word();
     if (!status) return PKV_ERR_CUDA;
-    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * (parts + 1);
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * (parts + ns);
     const size_t ml = (rows * sizeof(float) + 15) / 16 * 16;
     char* w = static_cast<char*>(workspace);
     float* o_part = reinterpret_cast<float*>(w);
@@ -363,7 +402,7 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
     pa.status = status;
     pa.num_blocks = pool->num_blocks;
     pa.max_blocks_per_seq = prefix_len / B;
-    pa.num_reqs = 1;
+    pa.num_reqs = ns;   // grid z: one per split of the prefix's tiles
     pa.total_new = num_seqs;
     pa.max_new = num_seqs;
     pa.num_q_heads = num_q_heads;
@@ -372,13 +411,32 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
     pa.cascade = 1;
     pa.cascade_keys = prefix_len;
     pa.cascade_rows = num_seqs;
-    pa.max_parts_total = parts + 1;
+    pa.cascade_tiles_per_split = tps;
+    pa.max_parts_total = parts + ns;
     pa.p_single_min_keys = prefill_p_single_min_keys();
     pa.o_part = o_part;
     pa.m_part = m_part;
     pa.l_part = l_part;
-    cudaError_t e = pkv::launch_paged_prefill(pa, group, st_);
+    // The prefix pass (tensor-bound, its K/V L2-resident) runs on a side stream beside
+    // the suffix decode (HBM-bound); the combine waits for both.
+    cudaStream_t side = side_stream();
+    if (!side) return PKV_ERR_CUDA;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventDestroy(fork);
+        return PKV_ERR_CUDA;
+    }
+    struct Events {   // released once their work completes
+        cudaEvent_t a, b;
+        ~Events() { cudaEventDestroy(a); cudaEventDestroy(b); }
+    } ev{fork, join};
+    if (cudaEventRecord(fork, st_) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    cudaError_t e = pkv::launch_paged_prefill(pa, group, side);
     if (e != cudaSuccess) return e == cudaErrorNotSupported ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
+    if (cudaEventRecord(join, side) != cudaSuccess) return PKV_ERR_CUDA;
 
     // 2. private suffixes (blocks from prefix_len / B on) + 3. log-sum-exp merge
     pkv::DecodeArgs a{};
@@ -402,10 +460,13 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
     a.m_part = m_part;
     a.l_part = l_part;
     a.chunk_offset = prefix_len / kChunk;
-    a.extra_parts = 1;
-    if (decode_use_simt())
-        return from_cuda(pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_));
-    return from_cuda(pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_));
+    a.extra_parts = ns;
+    a.defer_combine = 1;
+    e = decode_use_simt() ? pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_)
+                          : pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaStreamWaitEvent(st_, join, 0) != cudaSuccess) return PKV_ERR_CUDA;
+    return from_cuda(pkv::launch_decode_combine(a, pool->dtype, pool->head_dim, st_));
 }
 
 pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q,
