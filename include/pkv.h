@@ -25,7 +25,10 @@
  *    device memory on these paths (scratch is passed in as `workspace`).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    All device work is enqueued asynchronously on it; no call synchronises except
- *    pkv_read_device_status.
+ *    pkv_read_device_status.  The kernel calls may therefore be recorded with stream
+ *    capture into a CUDA graph and replayed (make one call outside capture first, so
+ *    that the per-device status word and side stream exist); pkv_paged_decode_cascade
+ *    forks onto a library-owned stream and joins back within the call.
  *  - Argument errors are detected on the host and returned synchronously before any
  *    launch.  A failed launch returns PKV_ERR_CUDA.  Conditions only the device can
  *    see (a slot or block id outside the pool, a pipeline wait that ran out of time)
