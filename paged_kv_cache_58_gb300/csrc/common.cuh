@@ -133,30 +133,12 @@ PKV_DEVINL void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, u
 
 // 2-D tiled tensor copy global -> shared through a tensor map (coordinates in
 // elements, innermost first).
-PKV_DEVINL void tma_load_2d(void* smem_dst, const void* tmap, int32_t x, int32_t y,
-                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
-        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
 PKV_DEVINL void tma_load_3d(void* smem_dst, const void* tmap, int32_t x, int32_t y, int32_t z,
                             uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
-
-PKV_DEVINL void tma_load_4d(void* smem_dst, const void* tmap, int32_t x, int32_t y, int32_t z,
-                            int32_t w, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
-        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
         : "memory");
 }
 

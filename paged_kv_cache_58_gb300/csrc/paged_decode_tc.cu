@@ -1,7 +1,7 @@
 // Paged decode for bf16 pools on the tensor cores (warp-level MMA).
 //
 // Same work split as the CUDA-core decode: grid (partition, kv head, sequence), 4
-// warps per CTA, warp w streams every 4th 16-token block of the partition through
+// warps per CTA, warp w streams every 4th 16-token chunk of the partition through
 // its own ring of shared-memory stages and keeps its own online-softmax state; the
 // CTA merges the 4 states; a log-sum-exp combine merges partitions (split-KV
 // decode, aifetchly SGLang guide, "Integrating FlashInfer").  The blocks are
@@ -18,9 +18,10 @@
 // wrong orientation and is transposed in registers with movmatrix; it is split into
 // bf16 hi + lo parts so the probabilities keep ~2^-17 relative precision.
 //
-// Staging: each block's K slab and V slab arrive as one TMA box each, with the 128-byte
+// Staging: the kernel walks 16-token chunks (a 16-token block, or half of a 32-token
+// one); each chunk's K slab and V slab arrive as one TMA box each, with the 128-byte
 // swizzle so that ldmatrix reads them without bank conflicts: for head_dim 128 a 4-D
-// box (the block's 16 rows x 256 B as 2 row groups x 2 column halves x 8 rows x 128 B),
+// box (the chunk's 16 rows x 256 B as 2 row groups x 2 column halves x 8 rows x 128 B),
 // for head_dim 64 a 16-row x 64-column box.  The warp stays converged throughout: the
 // stage waits vote across lanes and the copies are predicated, because reconverging a
 // diverged warp costs hundreds of cycles on a busy scheduler.

@@ -38,11 +38,13 @@
 // warps always find the next S ready.  One warp issues each stream (S_j, then P_j V_j,
 // then S_{j+2} once that P.V completed: MMAs with different accumulators are not
 // ordered against each other).  K and V stages (3 each) are released when their S and
-// P.V have run, so the gathers of later tiles are in flight.  Each 16-token block of
-// a tile arrives as ONE 4-D TMA box (the block's 16 rows x 256 B viewed as 2 row
-// groups x 2 column halves x 8 rows x 128 B, 128-byte swizzle), so a K/V tile lands as
-// [8-key group][column half][8 rows][128 B]: a valid K-major operand (8-row atoms 2 KB
-// apart) for S and MN-major operand (column halves 1 KB apart) for P.V.
+// P.V have run, so the gathers of later tiles are in flight.  Each 16-token chunk of
+// a tile (a 16-token block, or half of a 32-token one) arrives as ONE TMA box: at
+// head_dim 128 a 4-D box (the chunk's 16 rows x 256 B viewed as 2 row groups x 2 column
+// halves x 8 rows x 128 B, 128-byte swizzle), so a K/V tile lands as [8-key group]
+// [column half][8 rows][128 B]: a valid K-major operand (8-row atoms 2 KB apart) for S
+// and MN-major operand (column halves 1 KB apart) for P.V; at head_dim 64 a 16-row x
+// 64-column box, the tile one 64-column half with 8-row atoms 1 KB apart.
 //
 // Measured costs per 128-key tile on GB300 (clock64 traces and isolated probes): the
 // 24 N = 128 MMAs (8 for S, 16 for the hi + lo P.V) take the tensor pipe about 1700

@@ -37,31 +37,11 @@ PKV_DEVINL void tc_fence_after() {
 }
 
 // ------------------------------------------------------------------ MMA
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 inputs here), fp32
-// accumulate; issued by one thread.
-PKV_DEVINL void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                          bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-        : "memory");
-}
-
-// Same with the A operand read from TMEM (K-major: row i in lane i, two bf16 of
-// consecutive k per 32-bit column, lower k in the low half).
-PKV_DEVINL void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                             bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-        : "memory");
-}
-
-// Predicated forms (only the lane with `on` issues) for a converged issuing warp.
+// D[tmem] (+)= A * B, kind::f16 (bf16 inputs here), fp32 accumulate.  A comes from a
+// shared-memory descriptor (umma_bf16_if) or from TMEM (umma_bf16_ta_if: K-major, row i
+// in lane i, two bf16 of consecutive k per 32-bit column, lower k in the low half); B
+// from a shared-memory descriptor.  One thread issues: these are predicated forms that
+// a whole converged warp executes, only the lane with `on` issuing.
 PKV_DEVINL void umma_bf16_if(bool on, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                              uint32_t idesc, bool accumulate) {
     asm volatile(
@@ -84,21 +64,14 @@ PKV_DEVINL void umma_bf16_ta_if(bool on, uint32_t d_tmem, uint32_t a_tmem, uint6
         : "memory");
 }
 
+// Arrive once on `bar` when every tcgen05 operation the issuing thread issued so far
+// has completed (predicated as above).
 PKV_DEVINL void umma_commit_if(bool on, uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
         "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
             smem_u32(bar)),
         "r"(static_cast<uint32_t>(on))
-        : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far
-// has completed.
-PKV_DEVINL void umma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
         : "memory");
 }
 
@@ -118,19 +91,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 // K-major tiles: rows of 128 B, 8-row atoms of 1024 B, SBO = distance between atoms.
 // MN-major tiles: 64-element (128 B) MN chunks per row; LBO = distance between MN
 // chunks, SBO = distance between 8-row K groups.
-PKV_DEVINL uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-    d |= 1ull << 46;
-    d |= 2ull << 61;
-    return d;
-}
-
-// The same descriptor as two 32-bit halves, so that per-MMA offsets are one 32-bit add
-// on the low half (start address field, bits 0-13; shared-memory addresses stay below
-// 2^18, so the field never carries into the leading-offset field).
+// Built as two 32-bit halves, so that per-MMA offsets are one 32-bit add on the low
+// half (start address field, bits 0-13; shared-memory addresses stay below 2^18, so the
+// field never carries into the leading-offset field).
 PKV_DEVINL uint32_t smem_desc_sw128_lo(uint32_t saddr, uint32_t lbo) {
     return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
