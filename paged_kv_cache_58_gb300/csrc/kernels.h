@@ -62,6 +62,10 @@ struct DecodeArgs {
     int chunk_offset;
     int extra_parts;
     int defer_combine;   // nonzero: the launcher leaves the combine to the caller
+    // Test hook (tensor-core decode): nonzero makes warp 0 of CTA (0, 0, 0) arm its first
+    // stage for 16 bytes more than the stage's copies deliver, so that wait runs out of
+    // time (PKV_ERR_TIMEOUT) while every copy still lands.  Zero in normal use.
+    int test_stall;
     // Causal prefill on the CUDA-core kernel (fp32 pools): with cached_lens set the grid
     // is (max_new, kv head, request) and CTA (i, kvh, r) decodes new token i of request
     // r -- query row q_offsets[r] + i, keys 0 .. cached_lens[r] + i -- in one partition.

@@ -154,7 +154,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const int ci = my_first + i * kWarps;   // chunk: rows 16 (ci & mask) of its block
         const int row = ((bad ? kvh : phys * a.num_kv_heads + kvh) << a.chunk_shift) * kBlk +
                         (ci & ((1 << a.chunk_shift) - 1)) * kBlk;
-        mbar_arrive_expect_tx_if(on && !bad && lane == 0, bar, SM::kStageBytes);
+        const bool stall = a.test_stall && i == 0 && warp == 0 && blockIdx.x == 0 &&
+                           blockIdx.y == 0 && blockIdx.z == 0;
+        mbar_arrive_expect_tx_if(on && !bad && lane == 0, bar,
+                                 SM::kStageBytes + (stall ? 16u : 0u));
         const bool mine = on && !bad && lane < 2;
         uint8_t* dst = st + (lane == 1 ? SM::kSlab : 0);
         const void* map = lane == 1 ? static_cast<const void*>(&tm_v) : &tm_k;

@@ -15,11 +15,11 @@
 namespace {
 
 constexpr int kChunk = 16;   // the kernels walk sequences in 16-token chunks
+constexpr int kMaxDevices = 64;
+constexpr double kLog2e = 1.4426950408889634;
 
 // log2(block_size / 16) for the supported block sizes 16 and 32, else -1.
 int chunk_shift(int block_size) { return block_size == 16 ? 0 : block_size == 32 ? 1 : -1; }
-constexpr int kMaxDevices = 64;
-constexpr double kLog2e = 1.4426950408889634;
 
 // Library device status word: first error code raised by a kernel (0 = none).
 __device__ int g_pkv_status = 0;
@@ -119,6 +119,13 @@ constexpr int kPSingleMinKeys = 1024;
 int prefill_p_single_min_keys() {
     const char* v = std::getenv("PKV_PREFILL_P");
     return (v != nullptr && std::strcmp(v, "split") == 0) ? INT_MAX : kPSingleMinKeys;
+}
+
+// PKV_TEST_DECODE_STALL=1 arms the tensor-core decode's timeout test hook (one wait of
+// one warp runs out of time; read at each call; tests only).
+int decode_test_stall() {
+    const char* v = std::getenv("PKV_TEST_DECODE_STALL");
+    return v != nullptr && std::strcmp(v, "1") == 0;
 }
 
 size_t decode_workspace(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
@@ -277,8 +284,10 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
         a.l_part = reinterpret_cast<float*>(w + rows * pool->head_dim * sizeof(float) + ml);
     }
     const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
-    if (pool->dtype == PKV_BF16 && !decode_use_simt())
+    if (pool->dtype == PKV_BF16 && !decode_use_simt()) {
+        a.test_stall = decode_test_stall();
         return from_cuda(pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_));
+    }
     return from_cuda(pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_));
 }
 

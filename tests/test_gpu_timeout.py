@@ -1,0 +1,54 @@
+"""The bounded pipeline wait on a GPU: a wait that runs out of time reports
+PKV_ERR_TIMEOUT through the device status word and leaves the context usable.
+
+The test hook PKV_TEST_DECODE_STALL=1 makes one warp of one CTA of the tensor-core
+decode arm its first stage's barrier for 16 bytes more than that stage's copies
+deliver.  All copies land; the barrier phase never completes, so that warp's wait
+expires after its time budget (2 s), raises the status, drains its other stage and
+finishes.  Nothing faults, traps or loops without a limit."""
+import dataclasses
+
+import pytest
+import torch
+
+import synth
+from tests.helpers import check_attention, oracle_decode_case
+
+pytestmark = pytest.mark.gpu
+
+PKV_ERR_TIMEOUT = 4
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_58_gb300 as m
+    from paged_kv_cache_58_gb300 import build
+    build.build()
+    return m
+
+
+def test_decode_wait_timeout_reports_status(pkv, oracle_mod, monkeypatch):
+    monkeypatch.delenv("PKV_DECODE_KERNEL", raising=False)
+    wl = dataclasses.replace(synth.WORKLOADS["8b"], num_blocks=256)
+    case = synth.build_case(wl, "cuda", lengths=[100, 37, 300], seed=3)
+    pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+
+    def decode():
+        return pkv.paged_decode(case.q, case.k_pool, case.v_pool, case.block_tables,
+                                case.context_lens, case.scale, max_context=case.max_context)
+
+    monkeypatch.setenv("PKV_TEST_DECODE_STALL", "1")
+    decode()
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == PKV_ERR_TIMEOUT
+    # reading the status cleared it; the context still runs kernels correctly
+    monkeypatch.delenv("PKV_TEST_DECODE_STALL")
+    out = decode()
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    ref, _, _ = oracle_decode_case(oracle_mod, case)
+    check_attention(out, ref)
