@@ -1,8 +1,11 @@
 """Benchmark of the paged-KV decode hot path on GB300.
 
 A step is one pass of the hot path over one batch of the Llama-3-8B-shaped
-decode layer: kv_append of the batch's 64 new tokens, then paged_decode of the
-64 queries over their paged contexts (split-KV partitions + LSE combine).
+decode layer: kv_append of the batch's 64 new tokens and paged_decode of the
+64 queries over their paged contexts (split-KV partitions + LSE combine).  By
+default both run as one call, pkv_paged_decode_append (the decode kernel stores
+and attends the new tokens); --separate-append times kv_append followed by
+paged_decode instead.
 Inputs are seeded synthetic tensors already resident in HBM.  Prints ONE JSON
 line (rank 0).
 
@@ -50,6 +53,9 @@ def parse():
                    help="split-KV partition size in blocks (0: the library's policy)")
     p.add_argument("--cascade", action="store_true",
                    help="shared workload: decode with the shared-prefix cascade")
+    p.add_argument("--separate-append", action="store_true",
+                   help="time kv_append + paged_decode as two calls instead of the fused "
+                        "pkv_paged_decode_append")
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--prefill-steps", type=int, default=20)
     p.add_argument("--min-warm-seconds", type=float, default=1.0,
@@ -361,15 +367,28 @@ def main():
     launches_per_step = 2 + (1 if max_parts > 1 else 0)
 
     cascade = args.cascade and case.wl.shared_prefix > 0
+    fused = not cascade and not args.separate_append
     if cascade:
         plen = case.wl.shared_prefix
         prefix_blocks = case.block_tables[0, :plen // 16].contiguous()
         wsz = pkv.cascade_workspace_bytes(S, Hq, D, plen, max_ctx)
         workspace = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
         launches_per_step = 4
+    if fused:
+        launches_per_step -= 1
+        # The fused call reads no slot mapping: the table gives each new token's slot.
+        append_bytes -= case.slot_mapping.numel() * case.slot_mapping.element_size()
 
-    def decode(q, bt, cl):
-        if cascade:
+    def append(slots, kn, vn):
+        if not fused:
+            pkv.kv_append(case.k_pool, case.v_pool, slots, kn, vn, stream=stream)
+
+    def decode(q, bt, cl, kn=None, vn=None):
+        if fused:
+            pkv.paged_decode_append(q, case.k_pool, case.v_pool, kn, vn, bt, cl, case.scale,
+                                    max_context=max_ctx, out=out, partition_blocks=pb,
+                                    workspace=workspace, stream=stream)
+        elif cascade:
             pkv.paged_decode_cascade(q, case.k_pool, case.v_pool, prefix_blocks, plen, bt, cl,
                                      case.scale, max_context=max_ctx, out=out,
                                      workspace=workspace, stream=stream)
@@ -379,9 +398,8 @@ def main():
                              workspace=workspace, stream=stream)
 
     def step():
-        pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new,
-                      stream=stream)
-        decode(case.q, case.block_tables, case.context_lens)
+        append(case.slot_mapping, case.k_new, case.v_new)
+        decode(case.q, case.block_tables, case.context_lens, case.k_new, case.v_new)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -405,10 +423,9 @@ def main():
     torch.cuda.synchronize()
     start.record(stream)
     for i in range(K):
-        pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new,
-                      stream=stream)
+        append(case.slot_mapping, case.k_new, case.v_new)
         ev[i][0].record(stream)
-        decode(case.q, case.block_tables, case.context_lens)
+        decode(case.q, case.block_tables, case.context_lens, case.k_new, case.v_new)
         ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -438,7 +455,9 @@ def main():
     if not args.no_e2e:
         # The step's inputs staged in one pinned host buffer (256-byte aligned pieces) and
         # moved by one host-to-device copy; the kernels read device views of it.
-        names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+        names = ("q", "k_new", "v_new", "block_tables", "context_lens")
+        if not fused:
+            names += ("slot_mapping",)
         srcs = [getattr(case, n).contiguous() for n in names]
         offs, total = [], 0
         for t in srcs:
@@ -458,9 +477,9 @@ def main():
 
         def e2e_step():
             dev_buf.copy_(host_buf, non_blocking=True)
-            pkv.kv_append(case.k_pool, case.v_pool, devb["slot_mapping"], devb["k_new"],
-                          devb["v_new"], stream=stream)
-            decode(devb["q"], devb["block_tables"], devb["context_lens"])
+            append(devb.get("slot_mapping"), devb["k_new"], devb["v_new"])
+            decode(devb["q"], devb["block_tables"], devb["context_lens"], devb["k_new"],
+                   devb["v_new"])
             out_h.copy_(out, non_blocking=True)
             stream.synchronize()
 
@@ -484,8 +503,10 @@ def main():
 
     peak, tpeak, peak_kind = peaks()
     # Roofline on the unique bytes: a shared prefix is read from HBM once per step and
-    # from L2 by every other sequence, so the logical rate can exceed HBM bandwidth.
-    achieved = unique_bytes / (decode_ms * 1e-3) / 1e9
+    # from L2 by every other sequence, so the logical rate can exceed HBM bandwidth.  The
+    # fused call also moves the new rows (read from the input, stored into the pool).
+    call_bytes = unique_bytes + (append_bytes if fused else 0)
+    achieved = call_bytes / (decode_ms * 1e-3) / 1e9
     traffic = None
     if args.workload == "8b" and case.q.dtype.itemsize == 2:
         csrc = os.path.join(ROOT, "paged_kv_cache_58_gb300", "csrc")
@@ -512,13 +533,20 @@ def main():
                    "l2": ("inputs larger than L2 (K/V read per step > 129 MB L2)"
                           if decode_bytes > 2 * 129e6 else
                           "K/V per step smaller than L2: warm-cache figure"),
-                   "parallelism": f"replicas x{ws}", "cascade": cascade},
+                   "parallelism": f"replicas x{ws}", "cascade": cascade,
+                   "step": ("paged_decode_append (append fused into the decode)" if fused
+                            else "kv_append + " + ("paged_decode_cascade" if cascade
+                                                   else "paged_decode"))},
         "roofline": {"bound": "hbm",
                      "kernel": ("paged_decode_cascade (prefix pass + suffix split-KV + combine)"
-                                if cascade else "paged_decode (decode_tc split-KV + combine)"),
+                                if cascade else
+                                "paged_decode_append (decode_tc split-KV with the append "
+                                "+ combine)" if fused else
+                                "paged_decode (decode_tc split-KV + combine)"),
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "bytes_per_launch": unique_bytes,
-                     "logical_gbs": decode_bytes / (decode_ms * 1e-3) / 1e9,
+                     "bytes_per_launch": call_bytes,
+                     "logical_gbs": (decode_bytes + (append_bytes if fused else 0)) /
+                                    (decode_ms * 1e-3) / 1e9,
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "decode_ms": decode_ms, "traffic": traffic},

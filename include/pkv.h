@@ -124,6 +124,29 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
                             int num_q_heads, float scale, int partition_blocks,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* kv_append and paged_decode of one decode step in one pass.  k_new / v_new hold the K /
+ * V of each sequence's newest token, position context_lens[s] - 1; it goes to the slot
+ * that position has in the block table, block_tables[s][(L - 1) / block_size] at offset
+ * (L - 1) % block_size: the next slot of the sequence, which appending fills (Triptych
+ * page, "Paged Attention for Efficient Memory Management").  The decode CTA whose chunk
+ * holds that position stores the token into the pool and attends it straight from
+ * k_new / v_new, so no append launch precedes the decode.  Pools and output equal those
+ * of pkv_kv_append with those slots followed by pkv_paged_decode.
+ *   k_new, v_new    device [num_seqs][num_kv_heads][head_dim], pool dtype, 16-byte
+ *                   aligned; read only.
+ *   k_pool, v_pool  written at the new tokens' slots only.
+ * Each sequence's new slot must be its own (not reached through another sequence's table:
+ * copy-on-write of a shared last block, pkv_alloc_append, guarantees that).  A table entry
+ * outside [0, num_blocks) for the new slot skips its store and raises PKV_ERR_OOB in the
+ * device status word.  Other arguments, errors and the workspace as pkv_paged_decode. */
+pkv_status pkv_paged_decode_append(const pkv_pool_desc* pool, void* out, const void* q,
+                                   void* k_pool, void* v_pool, const void* k_new,
+                                   const void* v_new, const int32_t* block_tables,
+                                   int max_blocks_per_seq, const int32_t* context_lens,
+                                   int max_context, int num_seqs, int num_q_heads, float scale,
+                                   int partition_blocks, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
 /* Partition size (in blocks) pkv_paged_decode uses for partition_blocks == 0; it
  * depends only on these arguments (0 for invalid ones). */
 int pkv_paged_decode_auto_partition(int num_seqs, int num_q_heads, int max_context,

@@ -65,6 +65,10 @@ def _load():
     lib.pkv_paged_decode.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, ctypes.c_int, vp,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, f32, ctypes.c_int,
                                      vp, sz, vp]
+    lib.pkv_paged_decode_append.restype = ctypes.c_int
+    lib.pkv_paged_decode_append.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, vp, vp,
+                                            ctypes.c_int, vp, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, f32, ctypes.c_int, vp, sz, vp]
     lib.pkv_paged_prefill.restype = ctypes.c_int
     lib.pkv_paged_prefill.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32,
@@ -237,6 +241,33 @@ def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *, max_co
                                   int(max_context), S, Hq, float(scale), int(partition_blocks),
                                   wptr, wbytes, _stream(stream))
     _check("pkv_paged_decode", st)
+    return out
+
+
+def paged_decode_append(q, k_pool, v_pool, k_new, v_new, block_tables, context_lens, scale, *,
+                        max_context, out=None, partition_blocks=0, workspace=None, stream=None):
+    """kv_append + paged_decode in one pass: k_new / v_new [S, Hkv, D] are the K / V of
+    each sequence's token context_lens[s] - 1, stored into the slot the block table gives
+    for that position and attended; returns out [S, Hq, D]."""
+    d = pool_desc(k_pool)
+    S, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    need = decode_workspace_bytes(S, Hq, D, max_context, partition_blocks, d.block_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wptr = workspace.data_ptr() if workspace is not None else None
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if tuple(k_new.shape) != (S, d.num_kv_heads, D) or tuple(v_new.shape) != tuple(k_new.shape):
+        raise ValueError("k_new / v_new must be [num_seqs, num_kv_heads, head_dim]")
+    st = _load().pkv_paged_decode_append(
+        ctypes.byref(d), _dev(out, "out", q.dtype), _dev(q, "q", k_pool.dtype),
+        _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
+        _dev(k_new, "k_new", k_pool.dtype), _dev(v_new, "v_new", k_pool.dtype),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), int(max_context), S, Hq, float(scale),
+        int(partition_blocks), wptr, wbytes, _stream(stream))
+    _check("pkv_paged_decode_append", st)
     return out
 
 

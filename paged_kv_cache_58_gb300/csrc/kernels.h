@@ -66,6 +66,13 @@ struct DecodeArgs {
     // stage for 16 bytes more than the stage's copies deliver, so that wait runs out of
     // time (PKV_ERR_TIMEOUT) while every copy still lands.  Zero in normal use.
     int test_stall;
+    // Fused append (decode only): non-null k_new / v_new ([num_seqs][Hkv][D], pool
+    // dtype) are the K / V of each sequence's newest token, position context_lens[s] - 1.
+    // The CTA whose chunk holds that position stores them into the pool slot the block
+    // table gives for it and uses them in place of the row it staged from the pool (which
+    // the append has not reached yet).
+    const void* k_new;
+    const void* v_new;
     // Causal prefill on the CUDA-core kernel (fp32 pools): with cached_lens set the grid
     // is (max_new, kv head, request) and CTA (i, kvh, r) decodes new token i of request
     // r -- query row q_offsets[r] + i, keys 0 .. cached_lens[r] + i -- in one partition.

@@ -121,6 +121,30 @@ PKV_DEVINL float reduce_scatter16(float (&v)[G], int lane) {
     }
 }
 
+// Fused append: the new token, row `r` of chunk `blk` (of sequence `seq`, kv head
+// `kvh`), replaces that row in the staged K and V slabs and is stored into its pool slot:
+// a plain copy of the bits kv_append writes.  Lane p handles 16-byte pieces p, p + 32, ..
+// of the K row then the V row (kPieces per row).  Kept out of line: it runs once per
+// sequence and kv head, and inlined it costs the streaming loop registers.
+template <int kPieces>
+__device__ __noinline__ void append_row(const void* k_new, const void* v_new, void* k_pool,
+                                        void* v_pool, uint8_t* stage, int slab_bytes, int phys,
+                                        int64_t num_blocks, int num_kv_heads, int chunk_shift,
+                                        int seq, int kvh, int blk, int r, int lane) {
+    const size_t row = ((((static_cast<size_t>(phys) * num_kv_heads + kvh) << chunk_shift) +
+                         (blk & ((1 << chunk_shift) - 1))) * kBlock) + r;
+    const size_t src = (static_cast<size_t>(seq) * num_kv_heads + kvh) * kPieces;
+    for (int p = lane; p < 2 * kPieces; p += 32) {
+        const int which = p / kPieces;
+        const int pc = p % kPieces;
+        const uint4 x = __ldg(static_cast<const uint4*>(which ? v_new : k_new) + src + pc);
+        reinterpret_cast<uint4*>(stage + which * slab_bytes)[r * kPieces + pc] = x;
+        if (phys >= 0 && phys < num_blocks)
+            static_cast<uint4*>(which ? v_pool : k_pool)[row * kPieces + pc] = x;
+    }
+    fence_proxy_async_smem();
+}
+
 template <typename T, int D, int G>
 struct DecodeSmem {
     static constexpr int kSlab = kBlock * D * static_cast<int>(sizeof(T));
@@ -158,9 +182,11 @@ decode_split_kernel(const DecodeArgs a) {
     int L = pre ? a.cached_lens[seq] + static_cast<int>(blockIdx.x) + 1 : a.context_lens[seq];
     const int span_end = a.chunk_offset + a.max_parts * a.partition_chunks;  // chunks covered
     const int max_chunks = a.max_blocks_per_seq << a.chunk_shift;
+    bool append = a.k_new != nullptr && !pre;
     if (L > max_chunks * kBlock || L > span_end * kBlock) {
         if (part == 0 && threadIdx.x == 0) raise_status(a.status, PKV_ERR_OOB);
         L = min(max_chunks, span_end) * kBlock;
+        append = false;   // the clamped end is not the new token
     }
     const int nblk = (L + kBlock - 1) / kBlock;
     const int b0 = a.chunk_offset + part * a.partition_chunks;
@@ -255,6 +281,13 @@ decode_split_kernel(const DecodeArgs a) {
         const T* V = reinterpret_cast<const T*>(ring + st_i * SM::kStageBytes + SM::kSlab);
         const int blk = my_first + i * kWarps;
         const int valid = min(kBlock, L - blk * kBlock);
+        if (append && blk == nblk - 1) {
+            append_row<D * static_cast<int>(sizeof(T)) / 16>(
+                a.k_new, a.v_new, const_cast<void*>(a.k_pool), const_cast<void*>(a.v_pool),
+                ring + st_i * SM::kStageBytes, SM::kSlab, __ldg(bt + (blk >> a.chunk_shift)),
+                a.num_blocks, a.num_kv_heads, a.chunk_shift, seq, kvh, blk, valid - 1, lane);
+            __syncwarp();
+        }
 
         float sc[8];
 #pragma unroll

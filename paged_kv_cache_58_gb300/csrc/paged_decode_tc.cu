@@ -111,9 +111,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     int L = a.context_lens[seq];
     const int span_end = a.chunk_offset + a.max_parts * a.partition_chunks;  // chunks covered
     const int max_chunks = a.max_blocks_per_seq << a.chunk_shift;
+    bool append = a.k_new != nullptr;
     if (L > max_chunks * kBlk || L > span_end * kBlk) {
         if (part == 0 && threadIdx.x == 0) raise_status(a.status, PKV_ERR_OOB);
         L = min(max_chunks, span_end) * kBlk;
+        append = false;   // the clamped end is not the new token
     }
     const int nblk = (L + kBlk - 1) / kBlk;
     const int b0 = a.chunk_offset + part * a.partition_chunks;
@@ -222,16 +224,42 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const int blk = my_first + i * kWarps;
         const int valid = min(kBlk, L - blk * kBlk);
 
-        if (valid < kBlk) {
+        const bool fuse = append && blk == nblk - 1;   // holds the new token, row valid - 1
+        if (valid < kBlk || fuse) {
+            uint8_t* stage = ring + st_i * SM::kStageBytes;
             // Rows past the context may hold anything (NaN included): zero their V so
             // that a zero probability contributes exactly zero.
-            uint8_t* vrows = ring + st_i * SM::kStageBytes + SM::kSlab;
             for (int idx = lane; idx < (kBlk - valid) * SM::kHalves * 8; idx += 32) {
                 const int t = valid + idx / (SM::kHalves * 8);
                 const int c = idx % (SM::kHalves * 8);
-                *reinterpret_cast<uint4*>(vrows + (t >> 3) * SM::kHalves * kAtom +
-                                          (c >> 3) * kAtom + (t & 7) * 128 + ((c & 7) << 4)) =
+                *reinterpret_cast<uint4*>(stage + SM::kSlab +
+                                          (slab_addr<D>(kbase, t, c) - kbase)) =
                     make_uint4(0, 0, 0, 0);
+            }
+            if (fuse) {
+                // The new token: lane -> (K or V, 16-byte piece c) of its row; it replaces
+                // the staged row and is stored into the pool slot (a plain copy, the same
+                // bits kv_append writes).
+                constexpr int kPieces = D / 8;
+                const int phys = __ldg(bt + (blk >> a.chunk_shift));
+                if (lane < 2 * kPieces) {
+                    const int which = lane / kPieces;
+                    const int c = lane % kPieces;
+                    const uint4 x = __ldg(static_cast<const uint4*>(which ? a.v_new : a.k_new) +
+                                          (static_cast<size_t>(seq) * a.num_kv_heads + kvh) *
+                                              kPieces + c);
+                    *reinterpret_cast<uint4*>(stage + which * SM::kSlab +
+                                              (slab_addr<D>(kbase, valid - 1, c) - kbase)) = x;
+                    if (phys >= 0 && phys < a.num_blocks) {
+                        const size_t row =
+                            ((((static_cast<size_t>(phys) * a.num_kv_heads + kvh)
+                               << a.chunk_shift) + (blk & ((1 << a.chunk_shift) - 1))) * kBlk) +
+                            valid - 1;
+                        uint4* pool = static_cast<uint4*>(const_cast<void*>(which ? a.v_pool
+                                                                                  : a.k_pool));
+                        pool[row * kPieces + c] = x;
+                    }
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();

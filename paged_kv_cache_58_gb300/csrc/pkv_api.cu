@@ -225,12 +225,15 @@ size_t pkv_paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_
     return decode_workspace(num_seqs, num_q_heads, head_dim, max_parts);
 }
 
-pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
-                            const void* k_pool, const void* v_pool,
-                            const int32_t* block_tables, int max_blocks_per_seq,
-                            const int32_t* context_lens, int max_context, int num_seqs,
-                            int num_q_heads, float scale, int partition_blocks,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+// pkv_paged_decode, and with k_new / v_new set pkv_paged_decode_append.
+pkv_status decode_impl(const pkv_pool_desc* pool, void* out, const void* q, const void* k_pool,
+                       const void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int max_context, int num_seqs,
+                       int num_q_heads, float scale, int partition_blocks, void* workspace,
+                       size_t workspace_bytes, const void* k_new, const void* v_new,
+                       void* stream) {
     pkv_status st = check_pool(pool);
     if (st != PKV_OK) return st;
     if (num_seqs < 0 || num_q_heads <= 0 || partition_blocks < 0) return PKV_ERR_INVALID;
@@ -275,6 +278,8 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
     a.partition_chunks = pb << a.chunk_shift;
     a.max_parts = max_parts;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    a.k_new = k_new;
+    a.v_new = v_new;
     if (need > 0) {
         const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
         const size_t ml = (rows * sizeof(float) + 15) / 16 * 16;
@@ -289,6 +294,33 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
         return from_cuda(pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_));
     }
     return from_cuda(pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_));
+}
+
+}  // namespace
+
+pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
+                            const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int max_context, int num_seqs,
+                            int num_q_heads, float scale, int partition_blocks,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_impl(pool, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                       context_lens, max_context, num_seqs, num_q_heads, scale,
+                       partition_blocks, workspace, workspace_bytes, nullptr, nullptr, stream);
+}
+
+pkv_status pkv_paged_decode_append(const pkv_pool_desc* pool, void* out, const void* q,
+                                   void* k_pool, void* v_pool, const void* k_new,
+                                   const void* v_new, const int32_t* block_tables,
+                                   int max_blocks_per_seq, const int32_t* context_lens,
+                                   int max_context, int num_seqs, int num_q_heads, float scale,
+                                   int partition_blocks, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+        return PKV_ERR_INVALID;
+    return decode_impl(pool, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                       context_lens, max_context, num_seqs, num_q_heads, scale,
+                       partition_blocks, workspace, workspace_bytes, k_new, v_new, stream);
 }
 
 pkv_status pkv_paged_decode_noalloc(const pkv_pool_desc* pool, void* out, const void* q,
