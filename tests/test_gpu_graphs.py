@@ -1,6 +1,7 @@
-"""Stream capture: a decode step (kv_append + paged_decode) and a cascade decode can be
-recorded into a CUDA graph and replayed -- the calls allocate nothing, read nothing back
-to the host and never synchronise -- and a replay gives the same bits as the eager calls.
+"""Stream capture: a decode step (kv_append + paged_decode, or the fused call) and a
+cascade decode can be recorded into a CUDA graph and replayed -- the calls allocate
+nothing, read nothing back to the host and never synchronise -- and a replay gives the
+same bits as the eager calls.
 The cascade's fork onto the library's side stream becomes part of the graph."""
 import dataclasses
 
@@ -61,6 +62,45 @@ def test_decode_step_graph_replay(pkv):
     torch.cuda.synchronize()
     assert pkv.read_device_status() == 0
     assert torch.equal(out_eager, out_graph)
+
+
+def test_fused_decode_step_graph_replay(pkv):
+    """The fused append + decode call captured and replayed: same output bits and the
+    same pool as the eager call, also after the new rows change."""
+    wl = dataclasses.replace(synth.WORKLOADS["8b"], num_seqs=16, num_blocks=4096)
+    case = synth.build_case(wl, "cuda", seed=35)
+    S, Hq, D = case.q.shape
+    max_ctx = case.max_context   # host bound, read before capturing
+    ws = torch.empty(max(pkv.decode_workspace_bytes(S, Hq, D, max_ctx), 16),
+                     dtype=torch.uint8, device="cuda")
+    out_eager = torch.empty_like(case.q)
+    out_graph = torch.empty_like(case.q)
+
+    def step(out):
+        pkv.paged_decode_append(case.q, case.k_pool, case.v_pool, case.k_new, case.v_new,
+                                case.block_tables, case.context_lens, case.scale,
+                                max_context=max_ctx, out=out, workspace=ws)
+
+    step(out_eager)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    g = capture(lambda: step(out_graph))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_eager, out_graph)
+    case.k_new.mul_(2.0)
+    case.v_new.mul_(-1.0)
+    step(out_eager)
+    torch.cuda.synchronize()
+    slots = case.slot_mapping
+    B = case.k_pool.shape[2]
+    blk, off = slots // B, slots % B
+    case.k_pool[blk, :, off] = 0   # the replay must store the new rows again
+    g.replay()
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    assert torch.equal(out_eager, out_graph)
+    assert torch.equal(case.k_pool[blk, :, off], case.k_new)
 
 
 def test_cascade_graph_replay(pkv):
