@@ -13,9 +13,10 @@ namespace pkv {
 // Launch `kern` with programmatic stream serialisation: its CTAs may be scheduled
 // while the previous kernel on the stream drains; every libpkv kernel starts with
 // griddep_wait(), so no input is read before the predecessor has completed.
+// With pdl false the launch is ordinary: no CTA is placed before the predecessor ends.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t stream, Args&&... args) {
+cudaError_t launch_maybe_pdl(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block,
+                             size_t smem, cudaStream_t stream, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -25,8 +26,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    return launch_maybe_pdl(true, kern, grid, block, smem, stream, std::forward<Args>(args)...);
 }
 
 // Upper bound on split-KV partitions of one sequence (combine kernel's smem).
@@ -62,6 +68,10 @@ struct DecodeArgs {
     int chunk_offset;
     int extra_parts;
     int defer_combine;   // nonzero: the launcher leaves the combine to the caller
+    // nonzero: the split kernel is launched without programmatic dependent launch, so its
+    // CTAs take no SM before the stream's previous kernel has ended (the cascade decode:
+    // the prefix pass on the side stream is placed first).
+    int no_pdl;
     // Test hook (tensor-core decode): nonzero makes warp 0 of CTA (0, 0, 0) arm its first
     // stage for 16 bytes more than the stage's copies deliver, so that wait runs out of
     // time (PKV_ERR_TIMEOUT) while every copy still lands.  Zero in normal use.

@@ -433,37 +433,55 @@ decode_combine_kernel(const DecodeArgs a) {
     if (np <= 0) return;
     const float* mp = a.m_part + row * total;
     const float* lp = a.l_part + row * total;
+    const float* op = a.o_part + row * total * D + lane * EL;
 
-    float M = -INFINITY;
-    for (int p = lane; p < np; p += 32) M = fmaxf(M, mp[p]);
+    // One round trip for the common case: m and l of partials lane and lane + 32 and the
+    // first 8 partial outputs are loaded together; the weights need the row max first.
+    auto load_o = [&](int p, float (&v)[EL]) {
+        const float* src = op + static_cast<size_t>(p) * D;
+        if constexpr (EL == 4) {
+            const float4 f = *reinterpret_cast<const float4*>(src);
+            v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        } else {
+            const float2 f = *reinterpret_cast<const float2*>(src);
+            v[0] = f.x; v[1] = f.y;
+        }
+    };
+    const float m_a = lane < np ? mp[lane] : -INFINITY;
+    const float l_a = lane < np ? lp[lane] : 0.f;
+    float v0[8][EL];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        if (u < np) load_o(u, v0[u]);
+    float M = m_a;
+    for (int p = lane + 32; p < np; p += 32) M = fmaxf(M, mp[p]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
-    const float* op = a.o_part + row * total * D + lane * EL;
     float acc[EL];
 #pragma unroll
     for (int e = 0; e < EL; ++e) acc[e] = 0.f;
-    float W = 0.f;
+    const float w_a = lane < np ? l_a * fast_exp2(m_a - M) : 0.f;
+    float W = w_a;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const float wu = __shfl_sync(0xffffffffu, w_a, u);
+        if (u < np) {
+#pragma unroll
+            for (int e = 0; e < EL; ++e) acc[e] = fmaf(wu, v0[u][e], acc[e]);
+        }
+    }
+    // Partials 8 .. np - 1 (long contexts), 8 loads in flight at a time.
     for (int base = 0; base < np; base += 32) {
         const int p = base + lane;
-        const float w = (p < np) ? lp[p] * fast_exp2(mp[p] - M) : 0.f;
-        W += w;
+        const float w = base == 0 ? w_a : ((p < np) ? lp[p] * fast_exp2(mp[p] - M) : 0.f);
+        if (base > 0) W += w;
         const int cnt = min(32, np - base);
-        for (int u0 = 0; u0 < cnt; u0 += 8) {
+        for (int u0 = base == 0 ? 8 : 0; u0 < cnt; u0 += 8) {
             float v[8][EL];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (u0 + u < cnt) {
-                    const float* src = op + static_cast<size_t>(base + u0 + u) * D;
-                    if constexpr (EL == 4) {
-                        const float4 f = *reinterpret_cast<const float4*>(src);
-                        v[u][0] = f.x; v[u][1] = f.y; v[u][2] = f.z; v[u][3] = f.w;
-                    } else {
-                        const float2 f = *reinterpret_cast<const float2*>(src);
-                        v[u][0] = f.x; v[u][1] = f.y;
-                    }
-                }
-            }
+            for (int u = 0; u < 8; ++u)
+                if (u0 + u < cnt) load_o(base + u0 + u, v[u]);
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const float wu = __shfl_sync(0xffffffffu, w, (u0 + u) & 31);
@@ -493,7 +511,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
         const unsigned gx = a.cached_lens ? static_cast<unsigned>(a.max_new)
                                           : static_cast<unsigned>(a.max_parts);
         dim3 grid(gx, a.num_kv_heads, a.num_seqs);
-        e = launch_pdl(kern, grid, dim3(kThreads), SM::kTotal, stream, a);
+        e = launch_maybe_pdl(!a.no_pdl, kern, grid, dim3(kThreads), SM::kTotal, stream, a);
         if (e != cudaSuccess) return e;
     }
     if (a.extra_parts == 0 && a.max_parts == 1) return e;  // output written directly

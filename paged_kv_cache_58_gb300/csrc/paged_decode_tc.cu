@@ -407,7 +407,8 @@ cudaError_t launch_tc(const DecodeArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (a.max_parts > 0) {   // zero when a cascade decode has no private suffix at all
         dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
-        e = launch_pdl(kern, grid, dim3(kThreads), SM::kTotal, stream, mk, mv, a);
+        e = launch_maybe_pdl(!a.no_pdl, kern, grid, dim3(kThreads), SM::kTotal, stream, mk, mv,
+                             a);
         if (e != cudaSuccess) return e;
     }
     if (a.extra_parts == 0 && a.max_parts == 1) return e;  // output written directly
