@@ -1,6 +1,6 @@
 // Paged decode for bf16 pools on the tensor cores (warp-level MMA).
 //
-// Same work split as the CUDA-core decode: grid (partition, kv head, sequence), 4
+// Same work split as the CUDA-core decode: one CTA per (partition, kv head, sequence), 4
 // warps per CTA, warp w streams every 4th 16-token chunk of the partition through
 // its own ring of shared-memory stages and keeps its own online-softmax state; the
 // CTA merges the 4 states; a log-sum-exp combine merges partitions (split-KV
@@ -102,9 +102,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
     griddep_wait();
     griddep_launch_dependents();
-    const int part = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int seq = blockIdx.z;
+    // Grid (kv head, sequence, partition), partition slowest: CTAs are placed in index
+    // order, so every sequence's first (mostly full-length) partition starts before any
+    // second one and the last wave holds only the short final partitions of the longest
+    // sequences: an approximate longest-first order that shortens the tail.
+    const int kvh = blockIdx.x;
+    const int seq = blockIdx.y;
+    const int part = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -406,7 +410,7 @@ cudaError_t launch_tc(const DecodeArgs& a, cudaStream_t stream) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
     if (e != cudaSuccess) return e;
     if (a.max_parts > 0) {   // zero when a cascade decode has no private suffix at all
-        dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
+        dim3 grid(a.num_kv_heads, a.num_seqs, a.max_parts);
         e = launch_maybe_pdl(!a.no_pdl, kern, grid, dim3(kThreads), SM::kTotal, stream, mk, mv,
                              a);
         if (e != cudaSuccess) return e;
