@@ -160,9 +160,21 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
+_POOL_DESCS: dict = {}
+
+
 def pool_desc(k_pool: torch.Tensor) -> PoolDesc:
-    nb, hkv, bs, d = k_pool.shape
-    return PoolDesc(nb, bs, hkv, d, _dtype_code(k_pool))
+    """The pool descriptor of a [num_blocks, Hkv, B, D] pool (cached per shape and dtype:
+    it holds sizes only)."""
+    key = (tuple(k_pool.shape), k_pool.dtype)
+    d = _POOL_DESCS.get(key)
+    if d is None:
+        nb, hkv, bs, dim = key[0]
+        d = PoolDesc(nb, bs, hkv, dim, _dtype_code(k_pool))
+        if len(_POOL_DESCS) > 64:
+            _POOL_DESCS.clear()
+        _POOL_DESCS[key] = d
+    return d
 
 
 def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
@@ -227,9 +239,10 @@ def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *, max_co
     S, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
-    need = decode_workspace_bytes(S, Hq, D, max_context, partition_blocks, d.block_size)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:   # the library checks a given workspace's size itself
+        need = decode_workspace_bytes(S, Hq, D, max_context, partition_blocks, d.block_size)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wptr = workspace.data_ptr() if workspace is not None else None
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = _load().pkv_paged_decode(ctypes.byref(d), _dev(out, "out", q.dtype),
@@ -253,9 +266,10 @@ def paged_decode_append(q, k_pool, v_pool, k_new, v_new, block_tables, context_l
     S, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
-    need = decode_workspace_bytes(S, Hq, D, max_context, partition_blocks, d.block_size)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:   # the library checks a given workspace's size itself
+        need = decode_workspace_bytes(S, Hq, D, max_context, partition_blocks, d.block_size)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wptr = workspace.data_ptr() if workspace is not None else None
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     if tuple(k_new.shape) != (S, d.num_kv_heads, D) or tuple(v_new.shape) != tuple(k_new.shape):

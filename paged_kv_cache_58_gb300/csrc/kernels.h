@@ -109,6 +109,9 @@ bool make_pool_map(CUtensorMap* m, const void* pool, int64_t rows, int head_dim)
 // 2 column halves, rows / 8 row groups}, box {64, 8, 2, 2} = 4 KB, landing in shared
 // memory as [row group][half][8 rows][128 B] with the 128-byte swizzle.
 bool make_pool_block_map(CUtensorMap* m, const void* pool, int64_t rows);
+// cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, bytes), made once per kernel and
+// device (later calls with no more bytes return at once).
+cudaError_t set_smem_once(const void* kern, int bytes);
 // q [tokens][Hq][head_dim] bf16 read as boxes of 64 columns x G heads x tok tokens.
 bool make_q_group_map(CUtensorMap* m, const void* q, int tokens, int hq, int head_dim, int G,
                       int tok);

@@ -504,8 +504,7 @@ template <typename T, int D, int G>
 cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
     using SM = DecodeSmem<T, D, G>;
     auto kern = decode_split_kernel<T, D, G>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SM::kTotal);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), SM::kTotal);
     if (e != cudaSuccess) return e;
     if (a.max_parts > 0) {   // zero when a cascade decode has no private suffix at all
         const unsigned gx = a.cached_lens ? static_cast<unsigned>(a.max_new)

@@ -407,7 +407,7 @@ cudaError_t launch_tc(const DecodeArgs& a, cudaStream_t stream) {
     if (!maps_ok) return cudaErrorInvalidValue;
     auto kern = decode_tc_kernel<D, G>;
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
+        set_smem_once(reinterpret_cast<const void*>(kern), SM::kTotal);
     if (e != cudaSuccess) return e;
     if (a.max_parts > 0) {   // zero when a cascade decode has no private suffix at all
         dim3 grid(a.num_kv_heads, a.num_seqs, a.max_parts);

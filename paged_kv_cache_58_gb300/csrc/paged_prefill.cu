@@ -588,7 +588,7 @@ cudaError_t launch_g(const PrefillArgs& a, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     auto kern = prefill_tcgen05_kernel<D, G>;
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GM::kSmemBytes);
+        set_smem_once(reinterpret_cast<const void*>(kern), GM::kSmemBytes);
     if (e != cudaSuccess) return e;
     constexpr int TOK = kRows / G;
     dim3 grid((a.max_new + TOK - 1) / TOK, a.num_kv_heads, a.num_reqs);
