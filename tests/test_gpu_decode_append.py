@@ -115,6 +115,24 @@ def test_fused_llama3_8b_full(pkv, oracle_mod, kernel):
     check_attention(out, ref)
 
 
+@pytest.mark.parametrize("wl_name,n_rows", [("70b", 24), ("shared", 64)])
+def test_fused_full_size_sampled(pkv, oracle_mod, wl_name, n_rows):
+    """The 70B long-context and shared-prefix batches at full size through the fused
+    call (as the bench times them); sampled (sequence, head) outputs vs the oracle and
+    every new slot stored."""
+    case = synth.build_case(wl_name, "cuda")
+    S, Hq = case.q.shape[:2]
+    want = synth.sample_rows(S, Hq, n_rows, seed=5)
+    ref, _, _ = oracle_decode_case(oracle_mod, case, want=want)
+    out = fused(pkv, case)
+    check_attention(out, ref, mask=want)
+    assert torch.isfinite(out.float()).all()
+    B = case.k_pool.shape[2]
+    blk, off = case.slot_mapping // B, case.slot_mapping % B
+    assert torch.equal(case.k_pool[blk, :, off], case.k_new)
+    assert torch.equal(case.v_pool[blk, :, off], case.v_new)
+
+
 def test_fused_out_of_range_new_block_raises_status(pkv):
     """A table entry past the pool for the new token's block: no store, status OOB."""
     wl = dataclasses.replace(synth.WORKLOADS["8b"], num_seqs=2, num_blocks=64)
