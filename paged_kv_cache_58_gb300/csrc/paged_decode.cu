@@ -189,14 +189,9 @@ decode_split_kernel(const DecodeArgs a) {
         append = false;   // the clamped end is not the new token
     }
     const int nblk = (L + kBlock - 1) / kBlock;
-    // The span's np = ceil(span / partition_chunks) partitions are equal pieces (each at
-    // most partition_chunks), not full partitions and a short remainder: CTAs of one
-    // sequence take equal time, which shortens the tail of the grid.
-    const int span = nblk - a.chunk_offset;   // chunks this kernel covers
-    const int np = span > 0 ? (span + a.partition_chunks - 1) / a.partition_chunks : 0;
-    if (L <= 0 || part >= np) return;   // uniform over the CTA, before any barrier
-    const int b0 = a.chunk_offset + static_cast<int>(static_cast<int64_t>(part) * span / np);
-    const int b1 = a.chunk_offset + static_cast<int>(static_cast<int64_t>(part + 1) * span / np);
+    const int b0 = a.chunk_offset + part * a.partition_chunks;
+    if (L <= 0 || b0 >= nblk) return;  // uniform over the CTA, before any barrier
+    const int b1 = min(nblk, b0 + a.partition_chunks);
     const int my_first = b0 + warp;
     const int my_count = my_first < b1 ? (b1 - my_first + kWarps - 1) / kWarps : 0;
 

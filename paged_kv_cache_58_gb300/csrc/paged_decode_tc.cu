@@ -112,6 +112,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.max_blocks_per_seq;
+    const int b0 = a.chunk_offset + part * a.partition_chunks;
+    const int my_first = b0 + warp;
+    // The partition's start does not depend on the context length, so the block ids of
+    // this warp's first 32 chunks are loaded together with it rather than after it (one
+    // dependent round trip less before the first copy); ids past the sequence's end are
+    // loaded from inside the table row and then ignored.
+    int ids0;
+    {
+        const int e = (my_first + lane * kWarps) >> a.chunk_shift;
+        ids0 = e < a.max_blocks_per_seq ? __ldg(bt + e) : -1;
+    }
     int L = a.context_lens[seq];
     const int span_end = a.chunk_offset + a.max_parts * a.partition_chunks;  // chunks covered
     const int max_chunks = a.max_blocks_per_seq << a.chunk_shift;
@@ -122,20 +134,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         append = false;   // the clamped end is not the new token
     }
     const int nblk = (L + kBlk - 1) / kBlk;
-    // The span's np = ceil(span / partition_chunks) partitions are equal pieces (each at
-    // most partition_chunks), not full partitions and a short remainder: CTAs of one
-    // sequence take equal time, which shortens the tail of the grid.
-    const int span = nblk - a.chunk_offset;   // chunks this kernel covers
-    const int np = span > 0 ? (span + a.partition_chunks - 1) / a.partition_chunks : 0;
-    if (L <= 0 || part >= np) return;   // uniform over the CTA, before any barrier
-    const int b0 = a.chunk_offset + static_cast<int>(static_cast<int64_t>(part) * span / np);
-    const int b1 = a.chunk_offset + static_cast<int>(static_cast<int64_t>(part + 1) * span / np);
-    const int my_first = b0 + warp;
+    if (L <= 0 || b0 >= nblk) return;  // uniform over the CTA, before any barrier
+    const int b1 = min(nblk, b0 + a.partition_chunks);
     const int my_count = my_first < b1 ? (b1 - my_first + kWarps - 1) / kWarps : 0;
 
     uint8_t* ring = smem + warp * kStages * SM::kStageBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kRing) + warp * kStages;
-    const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.max_blocks_per_seq;
 
     if (lane == 0) {   // once per CTA
         prefetch_tmap(&tm_k);
@@ -152,7 +156,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const int i = base + lane;
         ids = (i < my_count) ? __ldg(bt + ((my_first + i * kWarps) >> a.chunk_shift)) : -1;
     };
-    fetch_ids(0);
+    ids = lane < my_count ? ids0 : -1;
 
     // Stage i: lane 0 sets the byte count, lane 0 copies the K slab and lane 1 the V
     // slab; all lanes execute the predicated instructions (no branch).
