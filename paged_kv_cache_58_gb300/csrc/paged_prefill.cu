@@ -498,11 +498,13 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                     uint8_t* vrow = smem + GM::kOffV + (jt % kStagesV) * GM::kTileBytes +
                                     (row >> 3) * GM::kGroupBytes + (row & 7) * 128;
                     const uint4 z = make_uint4(0, 0, 0, 0);
+                    // the whole 128-byte row, its 16-byte pieces in rotated order so that
+                    // the 8 rows of an atom hit 8 different bank groups at each step
 #pragma unroll
                     for (int h = 0; h < GM::kHalves; ++h)
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<uint4*>(vrow + h * 1024 + (j << 4)) = z;
+                            *reinterpret_cast<uint4*>(vrow + h * 1024 + ((j ^ (row & 7)) << 4)) = z;
                 }
                 fence_proxy_async_smem();
             }
