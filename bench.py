@@ -367,7 +367,7 @@ def main():
     launches_per_step = 2 + (1 if max_parts > 1 else 0)
 
     cascade = args.cascade and case.wl.shared_prefix > 0
-    fused = not cascade and not args.separate_append
+    fused = not args.separate_append
     if cascade:
         plen = case.wl.shared_prefix
         prefix_blocks = case.block_tables[0, :plen // 16].contiguous()
@@ -375,7 +375,7 @@ def main():
         workspace = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
         launches_per_step = 4
     if fused:
-        launches_per_step -= 1
+        launches_per_step -= 1   # the append runs inside the (suffix) decode kernel
         # The fused call reads no slot mapping: the table gives each new token's slot.
         append_bytes -= case.slot_mapping.numel() * case.slot_mapping.element_size()
 
@@ -384,7 +384,11 @@ def main():
             pkv.kv_append(case.k_pool, case.v_pool, slots, kn, vn, stream=stream)
 
     def decode(q, bt, cl, kn=None, vn=None):
-        if fused:
+        if fused and cascade:
+            pkv.paged_decode_cascade_append(q, case.k_pool, case.v_pool, kn, vn, prefix_blocks,
+                                            plen, bt, cl, case.scale, max_context=max_ctx,
+                                            out=out, workspace=workspace, stream=stream)
+        elif fused:
             pkv.paged_decode_append(q, case.k_pool, case.v_pool, kn, vn, bt, cl, case.scale,
                                     max_context=max_ctx, out=out, partition_blocks=pb,
                                     workspace=workspace, stream=stream)
@@ -534,11 +538,13 @@ def main():
                           if decode_bytes > 2 * 129e6 else
                           "K/V per step smaller than L2: warm-cache figure"),
                    "parallelism": f"replicas x{ws}", "cascade": cascade,
-                   "step": ("paged_decode_append (append fused into the decode)" if fused
+                   "step": (("paged_decode_cascade_append" if cascade else
+                             "paged_decode_append") + " (append fused into the decode)" if fused
                             else "kv_append + " + ("paged_decode_cascade" if cascade
                                                    else "paged_decode"))},
         "roofline": {"bound": "hbm",
-                     "kernel": ("paged_decode_cascade (prefix pass + suffix split-KV + combine)"
+                     "kernel": ("paged_decode_cascade (prefix pass + suffix split-KV + combine"
+                                + (", append fused)" if fused else ")")
                                 if cascade else
                                 "paged_decode_append (decode_tc split-KV with the append "
                                 "+ combine)" if fused else

@@ -202,6 +202,23 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
                                     int num_q_heads, float scale, int partition_blocks,
                                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* Cascade decode with the step's append fused in, as pkv_paged_decode_append does for
+ * pkv_paged_decode: k_new / v_new [num_seqs][num_kv_heads][head_dim] hold each sequence's
+ * newest token, position context_lens[s] - 1, which must lie in the private suffix
+ * (context_lens[s] > prefix_len).  The suffix decode stores it into the slot the block
+ * table gives for that position and attends it from k_new / v_new.  A sequence whose
+ * newest token lies inside the shared prefix is not stored and raises PKV_ERR_INVALID in
+ * the device status word.  Other arguments, errors and the workspace as
+ * pkv_paged_decode_cascade. */
+pkv_status pkv_paged_decode_cascade_append(const pkv_pool_desc* pool, void* out, const void* q,
+                                           void* k_pool, void* v_pool, const void* k_new,
+                                           const void* v_new, const int32_t* prefix_blocks,
+                                           int prefix_len, const int32_t* block_tables,
+                                           int max_blocks_per_seq, const int32_t* context_lens,
+                                           int max_context, int num_seqs, int num_q_heads,
+                                           float scale, int partition_blocks, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- paged_prefill
  * Causal prefill of new tokens over a cached prefix ("computes only the unseen
  * suffix" while reusing the cached prefix's K/V: aitalk.it, "RadixAttention: A Tree

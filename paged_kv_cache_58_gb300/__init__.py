@@ -69,6 +69,11 @@ def _load():
     lib.pkv_paged_decode_append.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, vp, vp,
                                             ctypes.c_int, vp, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, f32, ctypes.c_int, vp, sz, vp]
+    lib.pkv_paged_decode_cascade_append.restype = ctypes.c_int
+    lib.pkv_paged_decode_cascade_append.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, vp, vp,
+                                                    ctypes.c_int, vp, ctypes.c_int, vp,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    f32, ctypes.c_int, vp, sz, vp]
     lib.pkv_paged_prefill.restype = ctypes.c_int
     lib.pkv_paged_prefill.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32,
@@ -312,6 +317,33 @@ def paged_decode_cascade(q, k_pool, v_pool, prefix_blocks, prefix_len, block_tab
         _dev(context_lens, "context_lens", torch.int32), int(max_context), S, Hq, float(scale),
         int(partition_blocks), workspace.data_ptr(), workspace.numel(), _stream(stream))
     _check("pkv_paged_decode_cascade", st)
+    return out
+
+
+def paged_decode_cascade_append(q, k_pool, v_pool, k_new, v_new, prefix_blocks, prefix_len,
+                                block_tables, context_lens, scale, *, max_context, out=None,
+                                partition_blocks=0, workspace=None, stream=None):
+    """Cascade decode with the append fused in: k_new / v_new [S, Hkv, D] are the K / V
+    of each sequence's token context_lens[s] - 1 (in its private suffix)."""
+    d = pool_desc(k_pool)
+    S, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        need = cascade_workspace_bytes(S, Hq, D, prefix_len, max_context, partition_blocks,
+                                       d.block_size)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if tuple(k_new.shape) != (S, d.num_kv_heads, D) or tuple(v_new.shape) != tuple(k_new.shape):
+        raise ValueError("k_new / v_new must be [num_seqs, num_kv_heads, head_dim]")
+    st = _load().pkv_paged_decode_cascade_append(
+        ctypes.byref(d), _dev(out, "out", q.dtype), _dev(q, "q", k_pool.dtype),
+        _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
+        _dev(k_new, "k_new", k_pool.dtype), _dev(v_new, "v_new", k_pool.dtype),
+        _dev(prefix_blocks, "prefix_blocks", torch.int32), int(prefix_len),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), int(max_context), S, Hq, float(scale),
+        int(partition_blocks), workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check("pkv_paged_decode_cascade_append", st)
     return out
 
 

@@ -190,7 +190,13 @@ decode_split_kernel(const DecodeArgs a) {
     }
     const int nblk = (L + kBlock - 1) / kBlock;
     const int b0 = a.chunk_offset + part * a.partition_chunks;
-    if (L <= 0 || b0 >= nblk) return;  // uniform over the CTA, before any barrier
+    if (L <= 0 || b0 >= nblk) {   // uniform over the CTA, before any barrier
+        // A fused append in a cascade decode needs the newest token in the private
+        // suffix; one inside the shared prefix is not stored: report it.
+        if (append && part == 0 && threadIdx.x == 0 && L > 0 && nblk <= a.chunk_offset)
+            raise_status(a.status, PKV_ERR_INVALID);
+        return;
+    }
     const int b1 = min(nblk, b0 + a.partition_chunks);
     const int my_first = b0 + warp;
     const int my_count = my_first < b1 ? (b1 - my_first + kWarps - 1) / kWarps : 0;

@@ -134,7 +134,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         append = false;   // the clamped end is not the new token
     }
     const int nblk = (L + kBlk - 1) / kBlk;
-    if (L <= 0 || b0 >= nblk) return;  // uniform over the CTA, before any barrier
+    if (L <= 0 || b0 >= nblk) {   // uniform over the CTA, before any barrier
+        // A fused append in a cascade decode needs the newest token in the private
+        // suffix; one inside the shared prefix is not stored: report it.
+        if (append && part == 0 && threadIdx.x == 0 && L > 0 && nblk <= a.chunk_offset)
+            raise_status(a.status, PKV_ERR_INVALID);
+        return;
+    }
     const int b1 = min(nblk, b0 + a.partition_chunks);
     const int my_count = my_first < b1 ? (b1 - my_first + kWarps - 1) / kWarps : 0;
 

@@ -390,13 +390,17 @@ size_t pkv_paged_decode_cascade_workspace_bytes(int num_seqs, int num_q_heads, i
     return rows * head_dim * sizeof(float) + 2 * ml;
 }
 
-pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const void* q,
-                                    const void* k_pool, const void* v_pool,
-                                    const int32_t* prefix_blocks, int prefix_len,
-                                    const int32_t* block_tables, int max_blocks_per_seq,
-                                    const int32_t* context_lens, int max_context, int num_seqs,
-                                    int num_q_heads, float scale, int partition_blocks,
-                                    void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+// pkv_paged_decode_cascade, and with k_new / v_new set pkv_paged_decode_cascade_append
+// (the suffix decode stores and attends each sequence's newest token).
+pkv_status cascade_impl(const pkv_pool_desc* pool, void* out, const void* q, const void* k_pool,
+                        const void* v_pool, const int32_t* prefix_blocks, int prefix_len,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* context_lens, int max_context, int num_seqs,
+                        int num_q_heads, float scale, int partition_blocks, void* workspace,
+                        size_t workspace_bytes, const void* k_new, const void* v_new,
+                        void* stream) {
     pkv_status st = check_pool(pool);
     if (st != PKV_OK) return st;
     if (num_seqs < 0 || num_q_heads <= 0 || partition_blocks < 0 || !(scale > 0.f))
@@ -510,11 +514,44 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
     a.extra_parts = ns;
     a.defer_combine = 1;
     a.no_pdl = 1;
+    a.k_new = k_new;
+    a.v_new = v_new;
     e = decode_use_simt() ? pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_)
                           : pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     if (cudaStreamWaitEvent(st_, join, 0) != cudaSuccess) return PKV_ERR_CUDA;
     return from_cuda(pkv::launch_decode_combine(a, pool->dtype, pool->head_dim, st_));
+}
+
+}  // namespace
+
+pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const void* q,
+                                    const void* k_pool, const void* v_pool,
+                                    const int32_t* prefix_blocks, int prefix_len,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int max_context, int num_seqs,
+                                    int num_q_heads, float scale, int partition_blocks,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+    return cascade_impl(pool, out, q, k_pool, v_pool, prefix_blocks, prefix_len, block_tables,
+                        max_blocks_per_seq, context_lens, max_context, num_seqs, num_q_heads,
+                        scale, partition_blocks, workspace, workspace_bytes, nullptr, nullptr,
+                        stream);
+}
+
+pkv_status pkv_paged_decode_cascade_append(const pkv_pool_desc* pool, void* out, const void* q,
+                                           void* k_pool, void* v_pool, const void* k_new,
+                                           const void* v_new, const int32_t* prefix_blocks,
+                                           int prefix_len, const int32_t* block_tables,
+                                           int max_blocks_per_seq, const int32_t* context_lens,
+                                           int max_context, int num_seqs, int num_q_heads,
+                                           float scale, int partition_blocks, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+        return PKV_ERR_INVALID;
+    return cascade_impl(pool, out, q, k_pool, v_pool, prefix_blocks, prefix_len, block_tables,
+                        max_blocks_per_seq, context_lens, max_context, num_seqs, num_q_heads,
+                        scale, partition_blocks, workspace, workspace_bytes, k_new, v_new,
+                        stream);
 }
 
 pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q,

@@ -73,3 +73,69 @@ def test_cascade_without_private_suffix(pkv, oracle_mod):
     ref, _, _ = oracle_decode_case(oracle_mod, case)
     casc, _ = run_both(pkv, case, 64)
     check_attention(casc, ref)
+
+
+def fused_cascade(pkv, case, prefix_len, partition_blocks=0):
+    prefix_blocks = case.block_tables[0, :prefix_len // 16].contiguous()
+    return pkv.paged_decode_cascade_append(case.q, case.k_pool, case.v_pool, case.k_new,
+                                           case.v_new, prefix_blocks, prefix_len,
+                                           case.block_tables, case.context_lens, case.scale,
+                                           max_context=case.max_context,
+                                           partition_blocks=partition_blocks)
+
+
+@pytest.mark.parametrize("hq,prefix,suffixes,pb", [
+    (32, 16, [1, 15, 16, 17, 100], 0),
+    (32, 160, [1, 2, 300, 64, 1000], 2),
+    (8, 64, [5, 33, 1, 200], 1),
+])
+def test_cascade_fused_append_matches_oracle_and_two_calls(pkv, oracle_mod, hq, prefix,
+                                                           suffixes, pb):
+    """pkv_paged_decode_cascade_append: the suffix decode stores and attends the newest
+    tokens; same pools and output bits as kv_append followed by the cascade decode."""
+    from tests.helpers import pool_equal
+    wl = dataclasses.replace(synth.WORKLOADS["shared"], num_seqs=len(suffixes), num_q_heads=hq,
+                             shared_prefix=prefix, num_blocks=1024)
+    a = synth.build_case(wl, "cuda", lengths=suffixes, seed=prefix + hq + 1)
+    b = synth.build_case(wl, "cuda", lengths=suffixes, seed=prefix + hq + 1)
+    ref, kp, vp = oracle_decode_case(oracle_mod, a)
+    out_f = fused_cascade(pkv, a, prefix, pb)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    assert pool_equal(a.k_pool, kp) and pool_equal(a.v_pool, vp)
+    check_attention(out_f, ref)
+    out_s, _ = run_both(pkv, b, prefix, pb)
+    assert torch.equal(out_f.view(torch.int16), out_s.view(torch.int16))
+    assert torch.equal(a.k_pool.view(torch.int16), b.k_pool.view(torch.int16))
+
+
+def test_cascade_fused_append_published_batch_sampled(pkv, oracle_mod):
+    case = synth.build_case("shared", "cuda")
+    S, Hq = case.q.shape[:2]
+    want = synth.sample_rows(S, Hq, 64, seed=12)
+    ref, _, _ = oracle_decode_case(oracle_mod, case, want=want)
+    out = fused_cascade(pkv, case, 4096)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    check_attention(out, ref, mask=want)
+    B = case.k_pool.shape[2]
+    blk, off = case.slot_mapping // B, case.slot_mapping % B
+    assert torch.equal(case.k_pool[blk, :, off], case.k_new)
+
+
+def test_cascade_fused_append_token_inside_prefix_is_reported(pkv):
+    """A sequence whose newest token lies in the shared prefix: nothing is stored into the
+    shared blocks and the device status reads PKV_ERR_INVALID."""
+    wl = dataclasses.replace(synth.WORKLOADS["shared"], num_seqs=3, shared_prefix=64,
+                             num_blocks=256)
+    case = synth.build_case(wl, "cuda", lengths=[0, 5, 0], seed=8)
+    shared = case.block_tables[0, :4].long()
+    k_before = case.k_pool[shared].clone()
+    fused_cascade(pkv, case, 64)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 1
+    assert pkv.read_device_status() == 0
+    assert torch.equal(case.k_pool[shared].view(torch.int16), k_before.view(torch.int16))
+    B = case.k_pool.shape[2]
+    s1 = int(case.slot_mapping[1])
+    assert torch.equal(case.k_pool[s1 // B, :, s1 % B], case.k_new[1])
