@@ -102,6 +102,15 @@ def test_prefill_and_cascade_checks(pkv):
         return cas(ctypes.byref(a["dt"]), A, A, A, A, a["prefix"], a["plen"], A, a["mbs"], A,
                    a["max_ctx"], a["S"], a["hq"], 0.1, 0, a["ws"], a["wsb"], None)
 
+    ca = lib.pkv_paged_decode_cascade_append
+
+    def cf(kn=A, vn=A, S=2):
+        return ca(ctypes.byref(d), A, A, A, A, kn, vn, A, 64, A, 8, A, 100, S, 32, 0.1, 0, A,
+                  1 << 20, None)
+
+    assert cf(S=0) == OK
+    assert cf(kn=None) == INVALID
+    assert cf(vn=U) == INVALID
     assert c(S=0) == OK
     assert c(plen=40) == INVALID                              # not a multiple of the block
     assert c(plen=128, max_ctx=100) == INVALID                # prefix longer than the context

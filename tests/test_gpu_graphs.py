@@ -130,3 +130,33 @@ def test_cascade_graph_replay(pkv):
     torch.cuda.synchronize()
     assert pkv.read_device_status() == 0
     assert torch.equal(out_eager, out_graph)
+
+
+def test_fused_cascade_graph_replay(pkv):
+    """The cascade decode with the append fused in, captured and replayed."""
+    wl = dataclasses.replace(synth.WORKLOADS["shared"], num_seqs=32, shared_prefix=512,
+                             num_blocks=4096)
+    case = synth.build_case(wl, "cuda", seed=37)
+    S, Hq, D = case.q.shape
+    max_ctx = case.max_context   # host bound, read before capturing
+    prefix_blocks = case.block_tables[0, :512 // 16].contiguous()
+    ws = torch.empty(max(pkv.cascade_workspace_bytes(S, Hq, D, 512, max_ctx), 16),
+                     dtype=torch.uint8, device="cuda")
+    out_eager = torch.empty_like(case.q)
+    out_graph = torch.empty_like(case.q)
+
+    def call(out):
+        pkv.paged_decode_cascade_append(case.q, case.k_pool, case.v_pool, case.k_new,
+                                        case.v_new, prefix_blocks, 512, case.block_tables,
+                                        case.context_lens, case.scale, max_context=max_ctx,
+                                        out=out, workspace=ws)
+
+    call(out_eager)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    g = capture(lambda: call(out_graph))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    assert torch.equal(out_eager, out_graph)
