@@ -479,6 +479,10 @@ def main():
         h2d = total
         d2h = out_h.numel() * out_h.element_size()
 
+        e2e_api = "torch H2D copy + " + ("paged_decode_cascade_append" if cascade and fused
+                                         else "kv_append + paged_decode_cascade" if cascade
+                                         else "kv_append + paged_decode") + " + torch D2H copy"
+
         def e2e_step():
             dev_buf.copy_(host_buf, non_blocking=True)
             append(devb.get("slot_mapping"), devb["k_new"], devb["v_new"])
@@ -486,6 +490,27 @@ def main():
                    devb["v_new"])
             out_h.copy_(out, non_blocking=True)
             stream.synchronize()
+
+        if fused and not cascade:
+            # The C ABI's host-buffer step: one packed pinned input buffer, one copy each way.
+            mbs = case.block_tables.shape[1]
+            lay = pkv.decode_step_layout(case.k_pool, S, Hq, mbs)
+            host_in = torch.empty(lay.bytes, dtype=torch.uint8).pin_memory()
+            pkv.pack_decode_step(host_in, lay, case.q.cpu(), case.k_new.cpu(), case.v_new.cpu(),
+                                 case.block_tables.cpu(), case.context_lens.cpu())
+            staging = torch.empty(pkv.decode_host_staging_bytes(case.k_pool, S, Hq, mbs, max_ctx,
+                                                                pb),
+                                  dtype=torch.uint8, device=dev)
+            h2d = lay.bytes
+            e2e_api = "pkv_paged_decode_append_host (one H2D copy, fused step, one D2H copy)"
+
+            def e2e_step():
+                pkv.paged_decode_append_host(case.k_pool, case.v_pool, host_in, out_h,
+                                             case.scale, num_seqs=S, num_q_heads=Hq,
+                                             max_blocks_per_seq=mbs, max_context=max_ctx,
+                                             staging=staging, partition_blocks=pb,
+                                             stream=stream)
+                stream.synchronize()
 
         for _ in range(max(3, args.warmup)):
             e2e_step()
@@ -496,7 +521,7 @@ def main():
             e2e_step()
         el = time.perf_counter() - t0
         e2e_rate, el = aggregate(el, step_bytes * K, ws, reducer)
-        e2e = {"value": e2e_rate / 1e9, "unit": "GB/s",
+        e2e = {"value": e2e_rate / 1e9, "unit": "GB/s", "api": e2e_api,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": el / K * 1e3, "tokens_per_s_per_layer": ws * S * K / el}
 

@@ -147,6 +147,40 @@ pkv_status pkv_paged_decode_append(const pkv_pool_desc* pool, void* out, const v
                                    int partition_blocks, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/* ---------------------------------------------------------------- decode step from host memory
+ * The fused decode step with its inputs and output in host memory: the step's inputs sit
+ * packed in one host buffer laid out as pkv_decode_step_layout gives (q, k_new, v_new,
+ * block_tables, context_lens, each at a 256-byte aligned offset, in the layouts
+ * pkv_paged_decode_append takes), so that they move in one host-to-device copy.
+ *   layout  out: byte offsets of the five arrays and the buffer's total size.
+ * Returns PKV_ERR_INVALID for bad sizes. */
+typedef struct pkv_step_layout {
+    uint64_t q, k_new, v_new, block_tables, context_lens, bytes;
+} pkv_step_layout;
+pkv_status pkv_decode_step_layout(const pkv_pool_desc* pool, int num_seqs, int num_q_heads,
+                                  int max_blocks_per_seq, pkv_step_layout* layout);
+
+/* Device staging the host step needs: the packed inputs, the output and the split-KV
+ * workspace (0 for invalid arguments). */
+size_t pkv_paged_decode_append_host_staging_bytes(const pkv_pool_desc* pool, int num_seqs,
+                                                  int num_q_heads, int max_blocks_per_seq,
+                                                  int max_context, int partition_blocks);
+
+/* One decode step from host memory, queued on `stream`: a copy of host_in
+ * (layout.bytes bytes, packed as pkv_decode_step_layout says) into `staging` on the device,
+ * pkv_paged_decode_append on the staged arrays, and a copy of the output
+ * ([num_seqs][num_q_heads][head_dim], pool dtype) to host_out.  Host buffers should be
+ * pinned (page-locked) for the copies to run asynchronously; host_out is complete once
+ * the stream has been synchronised, and host_in must stay unchanged until then.
+ *   staging  device, >= pkv_paged_decode_append_host_staging_bytes(...) bytes, 256-byte
+ *            aligned; contents need no initialisation and are clobbered.
+ * Argument errors as pkv_paged_decode_append; PKV_ERR_NOMEM if staging is too small. */
+pkv_status pkv_paged_decode_append_host(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
+                                        const void* host_in, void* host_out,
+                                        int max_blocks_per_seq, int max_context, int num_seqs,
+                                        int num_q_heads, float scale, int partition_blocks,
+                                        void* staging, size_t staging_bytes, void* stream);
+
 /* Partition size (in blocks) pkv_paged_decode uses for partition_blocks == 0; it
  * depends only on these arguments (0 for invalid ones). */
 int pkv_paged_decode_auto_partition(int num_seqs, int num_q_heads, int max_context,

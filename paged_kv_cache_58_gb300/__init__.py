@@ -36,6 +36,13 @@ class PoolDesc(ctypes.Structure):
                 ("dtype", ctypes.c_int32)]
 
 
+class StepLayout(ctypes.Structure):
+    """Byte offsets of one decode step's inputs in a packed host buffer (and its size)."""
+    _fields_ = [("q", ctypes.c_uint64), ("k_new", ctypes.c_uint64), ("v_new", ctypes.c_uint64),
+                ("block_tables", ctypes.c_uint64), ("context_lens", ctypes.c_uint64),
+                ("bytes", ctypes.c_uint64)]
+
+
 _lib = None
 
 
@@ -74,6 +81,15 @@ def _load():
                                                     ctypes.c_int, vp, ctypes.c_int, vp,
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                     f32, ctypes.c_int, vp, sz, vp]
+    lib.pkv_decode_step_layout.restype = ctypes.c_int
+    lib.pkv_decode_step_layout.argtypes = [P(PoolDesc), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           P(StepLayout)]
+    lib.pkv_paged_decode_append_host_staging_bytes.restype = sz
+    lib.pkv_paged_decode_append_host_staging_bytes.argtypes = [P(PoolDesc)] + [ctypes.c_int] * 5
+    lib.pkv_paged_decode_append_host.restype = ctypes.c_int
+    lib.pkv_paged_decode_append_host.argtypes = [P(PoolDesc), vp, vp, vp, vp, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, f32,
+                                                 ctypes.c_int, vp, sz, vp]
     lib.pkv_paged_prefill.restype = ctypes.c_int
     lib.pkv_paged_prefill.argtypes = [P(PoolDesc), vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32,
@@ -288,6 +304,48 @@ def paged_decode_append(q, k_pool, v_pool, k_new, v_new, block_tables, context_l
         int(partition_blocks), wptr, wbytes, _stream(stream))
     _check("pkv_paged_decode_append", st)
     return out
+
+
+def decode_step_layout(k_pool, num_seqs, num_q_heads, max_blocks_per_seq) -> StepLayout:
+    """Packed host-buffer layout of one decode step's inputs (pkv_decode_step_layout)."""
+    lay = StepLayout()
+    _check("pkv_decode_step_layout",
+           _load().pkv_decode_step_layout(ctypes.byref(pool_desc(k_pool)), num_seqs, num_q_heads,
+                                          max_blocks_per_seq, ctypes.byref(lay)))
+    return lay
+
+
+def pack_decode_step(host_in, layout, q, k_new, v_new, block_tables, context_lens):
+    """Write one step's inputs (CPU tensors) into the packed host buffer `host_in` (uint8)."""
+    for off, t in ((layout.q, q), (layout.k_new, k_new), (layout.v_new, v_new),
+                   (layout.block_tables, block_tables), (layout.context_lens, context_lens)):
+        b = t.contiguous().view(torch.uint8).reshape(-1)
+        host_in[off:off + b.numel()].copy_(b)
+
+
+def decode_host_staging_bytes(k_pool, num_seqs, num_q_heads, max_blocks_per_seq, max_context,
+                              partition_blocks=0):
+    return int(_load().pkv_paged_decode_append_host_staging_bytes(
+        ctypes.byref(pool_desc(k_pool)), num_seqs, num_q_heads, max_blocks_per_seq, max_context,
+        partition_blocks))
+
+
+def paged_decode_append_host(k_pool, v_pool, host_in, host_out, scale, *, num_seqs, num_q_heads,
+                             max_blocks_per_seq, max_context, staging, partition_blocks=0,
+                             stream=None):
+    """One decode step from host memory: host_in (pinned uint8, packed as
+    decode_step_layout) -> device staging -> fused append + decode -> host_out (pinned
+    [S, Hq, D]).  Queued on the stream; host_out is complete after a synchronise."""
+    if host_in.is_cuda or host_out.is_cuda:
+        raise ValueError("host_in and host_out must be host tensors")
+    st = _load().pkv_paged_decode_append_host(
+        ctypes.byref(pool_desc(k_pool)), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool",
+                                                                       k_pool.dtype),
+        host_in.data_ptr(), host_out.data_ptr(), int(max_blocks_per_seq), int(max_context),
+        int(num_seqs), int(num_q_heads), float(scale), int(partition_blocks),
+        _dev(staging, "staging"), staging.numel() * staging.element_size(), _stream(stream))
+    _check("pkv_paged_decode_append_host", st)
+    return host_out
 
 
 def cascade_workspace_bytes(num_seqs, num_q_heads, head_dim, prefix_len, max_context,

@@ -328,6 +328,83 @@ pkv_status pkv_paged_decode_append(const pkv_pool_desc* pool, void* out, const v
                        partition_blocks, workspace, workspace_bytes, k_new, v_new, stream);
 }
 
+namespace {
+
+uint64_t round256(uint64_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+pkv_status pkv_decode_step_layout(const pkv_pool_desc* pool, int num_seqs, int num_q_heads,
+                                  int max_blocks_per_seq, pkv_step_layout* layout) {
+    pkv_status st = check_pool(pool);
+    if (st != PKV_OK) return st;
+    if (!layout || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0)
+        return PKV_ERR_INVALID;
+    const uint64_t row = static_cast<uint64_t>(pool->head_dim) * elem_bytes(pool->dtype);
+    const uint64_t S = static_cast<uint64_t>(num_seqs);
+    uint64_t off = 0;
+    layout->q = off;
+    off = round256(off + S * num_q_heads * row);
+    layout->k_new = off;
+    off = round256(off + S * pool->num_kv_heads * row);
+    layout->v_new = off;
+    off = round256(off + S * pool->num_kv_heads * row);
+    layout->block_tables = off;
+    off = round256(off + S * max_blocks_per_seq * sizeof(int32_t));
+    layout->context_lens = off;
+    off = round256(off + S * sizeof(int32_t));
+    layout->bytes = off;
+    return PKV_OK;
+}
+
+size_t pkv_paged_decode_append_host_staging_bytes(const pkv_pool_desc* pool, int num_seqs,
+                                                  int num_q_heads, int max_blocks_per_seq,
+                                                  int max_context, int partition_blocks) {
+    pkv_step_layout l;
+    if (pkv_decode_step_layout(pool, num_seqs, num_q_heads, max_blocks_per_seq, &l) != PKV_OK ||
+        num_seqs <= 0 || max_context <= 0 || partition_blocks < 0)
+        return 0;
+    const uint64_t out = round256(static_cast<uint64_t>(num_seqs) * num_q_heads *
+                                  pool->head_dim * elem_bytes(pool->dtype));
+    return l.bytes + out +
+           pkv_paged_decode_workspace_bytes(num_seqs, num_q_heads, pool->head_dim, max_context,
+                                            pool->block_size, partition_blocks);
+}
+
+pkv_status pkv_paged_decode_append_host(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
+                                        const void* host_in, void* host_out,
+                                        int max_blocks_per_seq, int max_context, int num_seqs,
+                                        int num_q_heads, float scale, int partition_blocks,
+                                        void* staging, size_t staging_bytes, void* stream) {
+    pkv_step_layout l;
+    pkv_status st = pkv_decode_step_layout(pool, num_seqs, num_q_heads, max_blocks_per_seq, &l);
+    if (st != PKV_OK) return st;
+    if (num_seqs == 0) return PKV_OK;
+    if (!host_in || !host_out || !staging || (reinterpret_cast<uintptr_t>(staging) & 255u))
+        return PKV_ERR_INVALID;
+    if (max_context <= 0 || partition_blocks < 0) return PKV_ERR_INVALID;
+    const size_t need = pkv_paged_decode_append_host_staging_bytes(
+        pool, num_seqs, num_q_heads, max_blocks_per_seq, max_context, partition_blocks);
+    if (need == 0) return PKV_ERR_INVALID;
+    if (staging_bytes < need) return PKV_ERR_NOMEM;
+    const uint64_t out_bytes = static_cast<uint64_t>(num_seqs) * num_q_heads * pool->head_dim *
+                               elem_bytes(pool->dtype);
+    char* dev = static_cast<char*>(staging);
+    char* out = dev + l.bytes;
+    char* ws = out + round256(out_bytes);
+    const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dev, host_in, l.bytes, cudaMemcpyHostToDevice, st_) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    st = pkv_paged_decode_append(pool, out, dev + l.q, k_pool, v_pool, dev + l.k_new,
+                                 dev + l.v_new, reinterpret_cast<const int32_t*>(dev + l.block_tables),
+                                 max_blocks_per_seq,
+                                 reinterpret_cast<const int32_t*>(dev + l.context_lens),
+                                 max_context, num_seqs, num_q_heads, scale, partition_blocks, ws,
+                                 need - (ws - dev), stream);
+    if (st != PKV_OK) return st;
+    return from_cuda(cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, st_));
+}
+
 pkv_status pkv_paged_decode_noalloc(const pkv_pool_desc* pool, void* out, const void* q,
                                     const void* k_pool, const void* v_pool,
                                     const int32_t* block_tables, int max_blocks_per_seq,

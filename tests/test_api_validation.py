@@ -117,3 +117,18 @@ def test_prefill_and_cascade_checks(pkv):
     assert c(prefix=None) == INVALID
     assert c(dt=desc(pkv, dtype=0)) == UNSUPPORTED            # bf16 only
     assert c(wsb=16) == NOMEM
+
+
+def test_host_step_checks(pkv):
+    lib = pkv.lib()
+    d = desc(pkv)
+    hs = lib.pkv_paged_decode_append_host
+
+    def h(hin=A, hout=A, stg=0x100000, stgb=1 << 24, S=2):
+        return hs(ctypes.byref(d), A, A, hin, hout, 8, 100, S, 32, 0.1, 0, stg, stgb, None)
+
+    assert h(S=0) == OK
+    assert h(hin=None) == INVALID
+    assert h(hout=None) == INVALID
+    assert h(stg=0x100010) == INVALID     # staging must be 256-byte aligned
+    assert h(stgb=64) == NOMEM

@@ -156,3 +156,31 @@ def test_fused_rejects_bad_new_rows(pkv):
         pkv.paged_decode_append(case.q, case.k_pool, case.v_pool, case.k_new[:1],
                                 case.v_new[:1], case.block_tables, case.context_lens,
                                 case.scale, max_context=case.max_context)
+
+
+@pytest.mark.parametrize("wl_name,lengths", [("8b", None), ("tiny", None),
+                                             ("8b", [1, 16, 17, 4000, 33])])
+def test_host_step_matches_device_call(pkv, wl_name, lengths):
+    """pkv_paged_decode_append_host (inputs and output in pinned host memory, one copy
+    each way) gives the device-buffer call's output bits and pools."""
+    kw = {} if lengths is None else {"lengths": lengths, "seed": 41}
+    a = synth.build_case(wl_name, "cuda", **kw)
+    b = synth.build_case(wl_name, "cuda", **kw)
+    S, Hq, D = a.q.shape
+    mbs = a.block_tables.shape[1]
+    out_dev = fused(pkv, b)
+    lay = pkv.decode_step_layout(a.k_pool, S, Hq, mbs)
+    host_in = torch.empty(lay.bytes, dtype=torch.uint8).pin_memory()
+    pkv.pack_decode_step(host_in, lay, a.q.cpu(), a.k_new.cpu(), a.v_new.cpu(),
+                         a.block_tables.cpu(), a.context_lens.cpu())
+    host_out = torch.empty((S, Hq, D), dtype=a.q.dtype).pin_memory()
+    staging = torch.empty(pkv.decode_host_staging_bytes(a.k_pool, S, Hq, mbs, a.max_context),
+                          dtype=torch.uint8, device="cuda")
+    pkv.paged_decode_append_host(a.k_pool, a.v_pool, host_in, host_out, a.scale, num_seqs=S,
+                                 num_q_heads=Hq, max_blocks_per_seq=mbs,
+                                 max_context=a.max_context, staging=staging)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    assert torch.equal(host_out.view(torch.uint8), out_dev.cpu().view(torch.uint8))
+    assert torch.equal(a.k_pool.view(torch.uint8), b.k_pool.view(torch.uint8))
+    assert torch.equal(a.v_pool.view(torch.uint8), b.v_pool.view(torch.uint8))

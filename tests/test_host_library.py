@@ -2,6 +2,7 @@
 
 No kernel is launched here; the library is loaded and only its host functions run.
 """
+import ctypes
 import json
 import os
 import re
@@ -205,3 +206,23 @@ def test_decode_workspace_and_partition_policy(pkv):
     assert pkv.auto_partition(16, 64, 131072, block_size=32) == 64
     # other block sizes are not supported
     assert pkv.auto_partition(64, 32, 4096, block_size=8) == 0
+
+
+def test_decode_step_layout(pkv):
+    """Packed host layout of a decode step: 256-byte aligned arrays in order, sizes from
+    the shapes; the staging adds the output and the split-KV workspace."""
+    d = pkv.PoolDesc(32768, 16, 8, 128, 1)
+    lay = pkv.StepLayout()
+    assert pkv.lib().pkv_decode_step_layout(ctypes.byref(d), 64, 32, 256, ctypes.byref(lay)) == 0
+    offs = [lay.q, lay.k_new, lay.v_new, lay.block_tables, lay.context_lens, lay.bytes]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert lay.q == 0 and lay.k_new >= 64 * 32 * 128 * 2
+    assert lay.v_new - lay.k_new >= 64 * 8 * 128 * 2
+    assert lay.context_lens - lay.block_tables >= 64 * 256 * 4
+    assert lay.bytes - lay.context_lens >= 64 * 4
+    staging = pkv.lib().pkv_paged_decode_append_host_staging_bytes(ctypes.byref(d), 64, 32,
+                                                                   256, 4096, 0)
+    assert staging == lay.bytes + 64 * 32 * 128 * 2 + pkv.decode_workspace_bytes(64, 32, 128,
+                                                                                 4096)
+    assert pkv.lib().pkv_decode_step_layout(ctypes.byref(d), -1, 32, 256,
+                                            ctypes.byref(lay)) == 1
