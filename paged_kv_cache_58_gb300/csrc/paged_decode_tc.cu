@@ -25,6 +25,11 @@
 // for head_dim 64 a 16-row x 64-column box.  The warp stays converged throughout: the
 // stage waits vote across lanes and the copies are predicated, because reconverging a
 // diverged warp costs hundreds of cycles on a busy scheduler.
+//
+// Fused append: with k_new / v_new set, the warp whose chunk holds a sequence's newest
+// token overwrites that token's staged K and V rows with the input rows (the pool does
+// not hold it yet) and stores the same bytes into the token's pool slot, so the step
+// needs no separate append launch.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
