@@ -64,3 +64,32 @@ def test_random_decode_config(pkv, oracle_mod, monkeypatch, i):
     assert torch.equal(a.k_pool.view(torch.uint8), b.k_pool.view(torch.uint8))
     assert torch.equal(out_f.view(torch.uint8), out_s.view(torch.uint8))
     check_attention(out_f, ref)
+
+
+def draw_prefill(i):
+    rng = np.random.default_rng(3000 + i)
+    hkv = int(rng.choice([1, 2, 8]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    d = int(rng.choice([64, 128]))
+    bs = int(rng.choice([16, 32]))
+    r = int(rng.integers(1, 5))
+    cached = [int(x) for x in rng.choice([0, 1, 15, 16, 100, 127, 128, 1000, 1024, 1500, 2100],
+                                         size=r)]
+    new = [int(x) for x in rng.choice([1, 2, 31, 32, 33, 100, 129, 300], size=r)]
+    return hkv, g, d, bs, cached, new
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_prefill_config(pkv, oracle_mod, i):
+    """tcgen05 prefill on drawn (requests, cached and new lengths, GQA group, head_dim,
+    block size): rows with 1024 keys or more take the single-P path, others the split."""
+    from tests.helpers import oracle_prefill_case
+    from tests.test_gpu_prefill import custom_case, run_prefill
+    hkv, g, d, bs, cached, new = draw_prefill(i)
+    nb = sum(-(-(c + n) // bs) for c, n in zip(cached, new)) + 64
+    case = custom_case(hkv * g, hkv, cached, new, seed=4000 + i, num_blocks=nb, head_dim=d,
+                       block_size=bs)
+    ref, kp, vp = oracle_prefill_case(oracle_mod, case)
+    out = run_prefill(pkv, case)
+    assert pool_equal(case.k_pool, kp) and pool_equal(case.v_pool, vp)
+    check_attention(out, ref)
