@@ -159,6 +159,18 @@ def test_zero_query_gives_mean_value(oracle_mod):
     np.testing.assert_allclose(out, V.astype(np.float64).mean(0), rtol=1e-12, atol=1e-15)
 
 
+def test_identical_keys_give_mean_value(oracle_mod):
+    """Every key the same: all scores equal whatever the query, so the weights are
+    uniform and the output is the mean of V (a scale applied to only some scores, or a
+    key index mixed up with a value index, breaks this)."""
+    rng = np.random.default_rng(13)
+    k = rng.standard_normal(16).astype(np.float32)
+    K = np.tile(k, (37, 1))
+    V = rng.standard_normal((37, 16)).astype(np.float32)
+    out = _single(oracle_mod, K, V, rng.standard_normal(16).astype(np.float32) * 4, 0.7)
+    np.testing.assert_allclose(out, V.astype(np.float64).mean(0), rtol=1e-12, atol=1e-15)
+
+
 def test_two_tokens_sigmoid_weights(oracle_mod):
     rng = np.random.default_rng(4)
     K = rng.standard_normal((2, 16)).astype(np.float32)
