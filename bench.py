@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode HBM GB/s (% of ~8 TB/s peak) and decode tokens/s per layer"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # 80.5
 DECODE_WORKLOADS = ("8b", "70b", "shared", "tiny")
 
 
@@ -56,6 +57,11 @@ def parse():
     p.add_argument("--separate-append", action="store_true",
                    help="time kv_append + paged_decode as two calls instead of the fused "
                         "pkv_paged_decode_append")
+    p.add_argument("--block-size", type=int, choices=[16, 32], default=0,
+                   help="tokens per pool block for the decode and prefill workloads "
+                        "(default: the recipe's 16; the pools keep their byte size)")
+    p.add_argument("--prefill-head-dim", type=int, choices=[64, 128], default=128)
+    p.add_argument("--prefill-dtype", choices=["bf16", "fp32"], default="bf16")
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--prefill-steps", type=int, default=20)
     p.add_argument("--min-warm-seconds", type=float, default=1.0,
@@ -94,13 +100,28 @@ def prefill_flops(case):
     return 4 * D * Hq * total
 
 
-def bench_prefill(pkv, dev, steps, stream):
+def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf16"):
     """Prefix-cached chunked prefill (16 requests x 512 new tokens over cached
     prefixes of U[1024, 8192]): kv_append of the new rows, then timed prefill calls
-    (CUDA events on the launching stream, K/V of 335 MB per call > L2)."""
+    (CUDA events on the launching stream, K/V of 335 MB per call > L2).  block_size,
+    head_dim and dtype vary the recipe (the pool keeps its byte size)."""
+    import dataclasses
     import torch
     import synth
-    case = synth.build_case("prefill", dev)
+    wl = synth.WORKLOADS["prefill"]
+    over = {}
+    if block_size and block_size != wl.block_size:
+        over.update(block_size=block_size,
+                    num_blocks=wl.num_blocks * wl.block_size // block_size)
+    if head_dim != wl.head_dim:
+        over.update(head_dim=head_dim)
+    if dtype == "fp32":
+        over.update(dtype=torch.float32)
+    if over:
+        wl = dataclasses.replace(wl, name=wl.name + "".join(
+            f"_{k}{v}" for k, v in (("B", over.get("block_size")), ("D", over.get("head_dim")),
+                                    ("", "f32" if dtype == "fp32" else None)) if v), **over)
+    case = synth.build_case(wl, dev)
     pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new,
                   stream=stream)
     out = torch.empty_like(case.q)
@@ -125,9 +146,11 @@ def bench_prefill(pkv, dev, steps, stream):
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     flops = prefill_flops(case)
     kv_bytes = int((case.context_lens.to(torch.int64)).sum()) * case.k_pool.shape[1] * \
-        case.q.shape[2] * 2 * 2
+        case.q.shape[2] * case.q.element_size() * 2
     res = {"workload": case.wl.name, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
-           "flops_per_call": flops, "kv_bytes_per_call": kv_bytes, "launches": steps}
+           "flops_per_call": flops, "kv_bytes_per_call": kv_bytes, "launches": steps,
+           "block_size": case.k_pool.shape[2], "head_dim": case.q.shape[2],
+           "dtype": "f32" if case.q.element_size() == 4 else "bf16"}
     del case, out
     return res
 
@@ -220,10 +243,11 @@ def workload_bytes(case):
     S, Hq, D = case.q.shape
     Hkv = case.k_pool.shape[1]
     esz = case.q.element_size()
+    B = case.k_pool.shape[2]   # tokens per pool block
     lens = case.context_lens.cpu().to(torch.int64)
     tokens = int(lens.sum())
     kv = tokens * Hkv * D * esz * 2
-    nblk = int(((lens + 15) // 16).sum())
+    nblk = int(((lens + B - 1) // B).sum())
     small = 2 * S * Hq * D * esz + nblk * 4 + S * 4
     decode = kv + small
     T = case.k_new.shape[0]
@@ -231,9 +255,9 @@ def workload_bytes(case):
     # distinct (block, row) slots: per physical block the most rows any sequence uses
     bt = case.block_tables.cpu().to(torch.int64)
     j = torch.arange(bt.shape[1])
-    nb = (lens + 15) // 16
+    nb = (lens + B - 1) // B
     used = j[None, :] < nb[:, None]
-    rows = (lens[:, None] - 16 * j[None, :]).clamp(0, 16)
+    rows = (lens[:, None] - B * j[None, :]).clamp(0, B)
     per_block = torch.zeros(case.k_pool.shape[0], dtype=torch.int64)
     per_block.scatter_reduce_(0, bt[used], rows[used], reduce="amax")
     unique_tokens = int(per_block.sum())
@@ -354,24 +378,31 @@ def main():
     if ws > 1:
         dist.barrier()
 
-    case = synth.build_case(args.workload, dev)
+    wl = synth.WORKLOADS[args.workload]
+    if args.block_size and args.block_size != wl.block_size:
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}_B{args.block_size}",
+                                 block_size=args.block_size,
+                                 num_blocks=wl.num_blocks * wl.block_size // args.block_size)
+    case = synth.build_case(wl, dev)
     S, Hq, D = case.q.shape
+    B = case.k_pool.shape[2]
     decode_bytes, append_bytes, tokens, unique_bytes = workload_bytes(case)
     max_ctx = case.max_context
-    pb = args.partition_blocks or pkv.auto_partition(S, Hq, max_ctx)
-    wsz = pkv.decode_workspace_bytes(S, Hq, D, max_ctx, pb)
+    pb = args.partition_blocks or pkv.auto_partition(S, Hq, max_ctx, block_size=B)
+    wsz = pkv.decode_workspace_bytes(S, Hq, D, max_ctx, pb, block_size=B)
     workspace = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
     out = torch.empty_like(case.q)
     stream = torch.cuda.current_stream(dev)
-    max_parts = math.ceil(math.ceil(max_ctx / 16) / pb)
+    max_parts = math.ceil(math.ceil(max_ctx / B) / pb)
     launches_per_step = 2 + (1 if max_parts > 1 else 0)
 
     cascade = args.cascade and case.wl.shared_prefix > 0
     fused = not args.separate_append
     if cascade:
         plen = case.wl.shared_prefix
-        prefix_blocks = case.block_tables[0, :plen // 16].contiguous()
-        wsz = pkv.cascade_workspace_bytes(S, Hq, D, plen, max_ctx)
+        prefix_blocks = case.block_tables[0, :plen // B].contiguous()
+        wsz = pkv.cascade_workspace_bytes(S, Hq, D, plen, max_ctx, block_size=B)
         workspace = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
         launches_per_step = 4
     if fused:
@@ -543,10 +574,19 @@ def main():
                                  os.path.join(ROOT, "profiles", "paged_decode_tc_llama3_8b.md"))
     prefill = None
     if not args.no_prefill:
-        prefill = bench_prefill(pkv, dev, args.prefill_steps, stream)
-        prefill.update({"bound": "tensor", "peak": tpeak, "unit": "TFLOP/s",
-                        "frac": prefill["tflops"] / tpeak,
-                        "peak_kind": f"{peak_kind} bf16_tflops (burst; kernel timed alone)"})
+        prefill = bench_prefill(pkv, dev, args.prefill_steps, stream, args.block_size,
+                                args.prefill_head_dim, args.prefill_dtype)
+        if prefill["dtype"] == "f32":
+            # fp32 pools run on the CUDA cores: fp32 FMA peak from the unit counts and the
+            # maximum SM clock (152 SMs x 128 FMA a clock x 2 flop x 2.07 GHz).
+            apeak = FP32_ALU_TFLOPS
+            prefill.update({"bound": "alu", "peak": apeak, "unit": "TFLOP/s",
+                            "frac": prefill["tflops"] / apeak,
+                            "peak_kind": "derived fp32 FMA peak (152 SMs x 128 x 2 x 2.07 GHz)"})
+        else:
+            prefill.update({"bound": "tensor", "peak": tpeak, "unit": "TFLOP/s",
+                            "frac": prefill["tflops"] / tpeak,
+                            "peak_kind": f"{peak_kind} bf16_tflops (burst; kernel timed alone)"})
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -554,7 +594,7 @@ def main():
         "pct_of_8tbs": 100.0 * value / ws / NOMINAL_HBM_GBS,
         "tokens_per_s_per_layer": tok_s,
         "config": {"workload": case.wl.name, "num_seqs": S, "q_heads": Hq,
-                   "kv_heads": case.k_pool.shape[1], "head_dim": D, "block_size": 16,
+                   "kv_heads": case.k_pool.shape[1], "head_dim": D, "block_size": B,
                    "pool_blocks": case.k_pool.shape[0], "mean_context": tokens / S,
                    "max_context": max_ctx, "partition_blocks": pb,
                    "kv_bytes_per_step": decode_bytes, "append_bytes_per_step": append_bytes,
