@@ -63,6 +63,8 @@ def parse():
     p.add_argument("--prefill-head-dim", type=int, choices=[64, 128], default=128)
     p.add_argument("--prefill-dtype", choices=["bf16", "fp32"], default="bf16")
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-prefix-cache", action="store_true",
+                   help="skip the host prefix-reuse measurement")
     p.add_argument("--prefill-steps", type=int, default=20)
     p.add_argument("--min-warm-seconds", type=float, default=1.0,
                    help="warm-up also runs at least this long (clock sampling under load)")
@@ -152,6 +154,53 @@ def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf
            "block_size": case.k_pool.shape[2], "head_dim": case.q.shape[2],
            "dtype": "f32" if case.q.element_size() == 4 else "bf16"}
     del case, out
+    return res
+
+
+def bench_prefix_cache(pkv, convs=32, turns=8, system=1024, per_turn=160, tail=64, reps=3):
+    """Host prefix reuse on a multi-turn agent workload (seeded): `convs` conversations
+    behind one shared `system`-token prompt; turn t's prompt is the system prompt plus
+    the conversation's first t * per_turn + tail tokens.  Each admission is the serving
+    flow through the binding: match, admit with the matched blocks shared, append the
+    rest, insert, free.  Reports admissions/s and the share of prompt tokens reused,
+    for the radix tree and for the chained block-hash cache."""
+    import random
+    rng = random.Random(58)
+    sys_prompt = [rng.randrange(32000) for _ in range(system)]
+    conv = [[rng.randrange(32000) for _ in range(turns * per_turn + tail)]
+            for _ in range(convs)]
+    order = [(t, c) for t in range(turns) for c in range(convs)]   # turns interleaved
+    res = {}
+    for kind in ("radix", "block_hash"):
+        best = None
+        for _ in range(reps):
+            alloc = pkv.BlockAllocator(16384)
+            cache = pkv.RadixTree(alloc) if kind == "radix" else pkv.PrefixCache(alloc)
+            reused = total = 0
+            t0 = time.perf_counter()
+            for sid, (t, c) in enumerate(order):
+                prompt = sys_prompt + conv[c][:t * per_turn + tail]
+                if kind == "radix":
+                    m, blocks = cache.match(prompt)
+                else:
+                    blocks = cache.match(prompt)
+                    m = len(blocks) * alloc.block_size
+                alloc.add_seq_shared(sid, blocks, m)
+                alloc.append(sid, len(prompt) - m)
+                cache.insert(sid, prompt)
+                alloc.free_seq(sid)
+                reused += m
+                total += len(prompt)
+            el = time.perf_counter() - t0
+            cache.close()
+            alloc.close()
+            if best is None or el < best:
+                best = el
+        res[kind] = {"admissions_per_s": len(order) / best, "reused_fraction": reused / total,
+                     "prompt_tokens": total}
+    res["workload"] = (f"{convs} conversations x {turns} turns, {system}-token shared system "
+                       f"prompt, +{per_turn} tokens a turn; one host thread through the "
+                       "Python binding")
     return res
 
 
@@ -623,6 +672,7 @@ def main():
                      "decode_ms": decode_ms, "traffic": traffic},
         "e2e": e2e,
         "prefill": prefill,
+        "prefix_cache": None if args.no_prefix_cache else bench_prefix_cache(pkv),
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }

@@ -10,6 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -513,8 +514,14 @@ class BlockAllocator:
 
 
 def _i32(values):
-    values = list(values)
-    return (ctypes.c_int32 * max(len(values), 1))(*values), len(values)
+    """Token ids as a contiguous int32 buffer for the C ABI: (pointer, count).  A numpy
+    conversion, not an element-by-element ctypes array (the pointer keeps its buffer
+    alive for the call)."""
+    a = np.ascontiguousarray(values, dtype=np.int32).reshape(-1)
+    n = int(a.size)
+    if n == 0:
+        a = np.zeros(1, dtype=np.int32)
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), n
 
 
 def block_hash(parent_hash: int, salt: int, tokens, extra: int = 0) -> int:
