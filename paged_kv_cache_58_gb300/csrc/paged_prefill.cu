@@ -447,7 +447,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const float p0 = fast_exp2(a0);
                         const float p1 = fast_exp2(a1);
                         const int u = (e & 3) * 2;
-                        fadd2(rs8[u], rs8[u + 1], rs8[u], rs8[u + 1], p0, p1);
+                        // row sums by fma with 1 (exact, one rounding as an add)
+                        ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
                         ph[e] = pack_bf16x2(p0, p1);
                     }
                     tmem_st16(tS + q * 16, ph);
@@ -464,7 +465,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const float p0 = fast_exp2(a0);
                     const float p1 = fast_exp2(a1);
                     const int u = (e & 3) * 2;
-                    fadd2(rs8[u], rs8[u + 1], rs8[u], rs8[u + 1], p0, p1);
+                    ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
                     phi[e] = pack_bf16x2_trunc(p0, p1);
                     float r0, r1;
                     ffma2(r0, r1, __uint_as_float(__float_as_uint(p0) & 0xffff0000u),
