@@ -83,13 +83,6 @@ struct DecodeArgs {
     // the append has not reached yet).
     const void* k_new;
     const void* v_new;
-    // Causal prefill on the CUDA-core kernel (fp32 pools): with cached_lens set the grid
-    // is (max_new, kv head, request) and CTA (i, kvh, r) decodes new token i of request
-    // r -- query row q_offsets[r] + i, keys 0 .. cached_lens[r] + i -- in one partition.
-    const int32_t* cached_lens;   // null: decode
-    const int32_t* new_lens;
-    const int32_t* q_offsets;
-    int max_new;
 };
 
 // CUDA-core decode (fp32 and bf16 pools): split kernel + combine.

@@ -166,23 +166,18 @@ decode_split_kernel(const DecodeArgs a) {
     griddep_wait();
     griddep_launch_dependents();
     const int kvh = blockIdx.y;
-    // Decode: CTA (partition, kvh, sequence).  Prefill: CTA (token i, kvh, request r),
-    // one partition, table row r, query / output row q_offsets[r] + i.
-    const bool pre = a.cached_lens != nullptr;
-    const int part = pre ? 0 : static_cast<int>(blockIdx.x);
+    const int part = blockIdx.x;
     const int seq = blockIdx.z;   // table row
-    if (pre && static_cast<int>(blockIdx.x) >= a.new_lens[seq]) return;   // uniform
-    const size_t qrow = pre ? static_cast<size_t>(a.q_offsets[seq]) + blockIdx.x
-                            : static_cast<size_t>(seq);
+    const size_t qrow = static_cast<size_t>(seq);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int hw = lane >> 4;   // half-warp: token parity
     const int c = lane & 15;    // D slice
 
-    int L = pre ? a.cached_lens[seq] + static_cast<int>(blockIdx.x) + 1 : a.context_lens[seq];
+    int L = a.context_lens[seq];
     const int span_end = a.chunk_offset + a.max_parts * a.partition_chunks;  // chunks covered
     const int max_chunks = a.max_blocks_per_seq << a.chunk_shift;
-    bool append = a.k_new != nullptr && !pre;
+    bool append = a.k_new != nullptr;
     if (L > max_chunks * kBlock || L > span_end * kBlock) {
         if (part == 0 && threadIdx.x == 0) raise_status(a.status, PKV_ERR_OOB);
         L = min(max_chunks, span_end) * kBlock;
@@ -513,9 +508,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), SM::kTotal);
     if (e != cudaSuccess) return e;
     if (a.max_parts > 0) {   // zero when a cascade decode has no private suffix at all
-        const unsigned gx = a.cached_lens ? static_cast<unsigned>(a.max_new)
-                                          : static_cast<unsigned>(a.max_parts);
-        dim3 grid(gx, a.num_kv_heads, a.num_seqs);
+        dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
         e = launch_maybe_pdl(!a.no_pdl, kern, grid, dim3(kThreads), SM::kTotal, stream, a);
         if (e != cudaSuccess) return e;
     }

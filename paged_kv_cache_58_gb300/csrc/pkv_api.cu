@@ -11,6 +11,7 @@
 
 #include "../../include/pkv.h"
 #include "kernels.h"
+#include "prefill_f32.h"
 
 namespace {
 
@@ -653,32 +654,6 @@ pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q
         return PKV_ERR_INVALID;
     int* status = status_word();
     if (!status) return PKV_ERR_CUDA;
-    if (pool->dtype == PKV_F32) {
-        // fp32 pools: each new token decoded on the CUDA-core kernel over keys 0 .. c + i
-        // (no tensor cores: fp32 operands would have to be rounded to tf32).
-        pkv::DecodeArgs d{};
-        d.out = out;
-        d.q = q;
-        d.k_pool = k_pool;
-        d.v_pool = v_pool;
-        d.block_tables = block_tables;
-        d.status = status;
-        d.num_blocks = pool->num_blocks;
-        d.max_blocks_per_seq = max_blocks_per_seq;
-        d.num_seqs = num_reqs;
-        d.num_q_heads = num_q_heads;
-        d.num_kv_heads = pool->num_kv_heads;
-        d.chunk_shift = chunk_shift(pool->block_size);
-        d.partition_chunks = max_blocks_per_seq << d.chunk_shift;   // one partition
-        d.max_parts = 1;
-        d.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
-        d.cached_lens = cached_lens;
-        d.new_lens = new_lens;
-        d.q_offsets = q_offsets;
-        d.max_new = max_new;
-        return from_cuda(pkv::launch_paged_decode(d, pool->dtype, pool->head_dim, group,
-                                                  static_cast<cudaStream_t>(stream)));
-    }
     pkv::PrefillArgs a{};
     a.head_dim = pool->head_dim;
     a.block_size = pool->block_size;
@@ -700,7 +675,11 @@ pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q
     a.num_kv_heads = pool->num_kv_heads;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     a.p_single_min_keys = prefill_p_single_min_keys();
-    const cudaError_t e = pkv::launch_paged_prefill(a, group, static_cast<cudaStream_t>(stream));
+    // fp32 pools run on the CUDA cores: the tensor cores would round fp32 operands to tf32.
+    const cudaError_t e =
+        pool->dtype == PKV_F32
+            ? pkv::launch_paged_prefill_f32(a, group, static_cast<cudaStream_t>(stream))
+            : pkv::launch_paged_prefill(a, group, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
     return from_cuda(e);
 }

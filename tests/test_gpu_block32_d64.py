@@ -140,9 +140,23 @@ def test_prefill_edges_d64_block32(pkv, oracle_mod, d, bs):
 @pytest.mark.parametrize("d,bs,hq,hkv", [(64, 16, 8, 2), (128, 16, 32, 8), (64, 32, 4, 4),
                                          (128, 32, 8, 1)])
 def test_prefill_fp32(pkv, oracle_mod, d, bs, hq, hkv):
-    """fp32 pools: every new token decoded on the CUDA-core kernel, causal."""
+    """fp32 pools: the tiled CUDA-core prefill, causal, fp32 throughout."""
     case = custom_case(hq, hkv, [0, 100, 33, 1], [37, 64, 17, 1], seed=d + bs + hq,
                        head_dim=d, block_size=bs, dtype=torch.float32)
+    ref, kp, vp = oracle_prefill_case(oracle_mod, case)
+    out = run_prefill(pkv, case)
+    assert pool_equal(case.k_pool, kp) and pool_equal(case.v_pool, vp)
+    max_abs, _ = check_attention(out, ref)
+    assert max_abs < 1e-5   # fp32 arithmetic throughout
+
+
+@pytest.mark.parametrize("d,bs,hq,hkv", [(128, 16, 32, 8), (64, 32, 16, 8), (128, 32, 8, 8),
+                                         (64, 16, 64, 8)])
+def test_prefill_fp32_multi_tile(pkv, oracle_mod, d, bs, hq, hkv):
+    """fp32 pools over several 64-row query tiles and 64-key KV tiles: ragged last tiles,
+    cached prefixes off every tile and block boundary, a one-token request, G 1 to 8."""
+    case = custom_case(hq, hkv, [0, 1000, 65, 4095, 63], [129, 300, 64, 1, 77],
+                       seed=7 * d + bs + hq, head_dim=d, block_size=bs, dtype=torch.float32)
     ref, kp, vp = oracle_prefill_case(oracle_mod, case)
     out = run_prefill(pkv, case)
     assert pool_equal(case.k_pool, kp) and pool_equal(case.v_pool, vp)
