@@ -183,7 +183,14 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     Ctl ctl{bars, abort_flag, a.status};
 
-    if (warp == kMmaWarp) {
+    // The producer warp sets up the barriers and starts the Q copy and the block-id loads
+    // of the first KV tiles before the CTA-wide barrier, beside the TMEM allocation.
+    const int32_t* bt =
+        a.block_tables + static_cast<size_t>(cascade ? 0 : r) * a.max_blocks_per_seq;
+    const int nchunks = max_lim / kChunk + 1;
+    const int csh = a.block_size == 32 ? 1 : 0;   // log2 of chunks per block
+    int ids = 0;   // producer: block id of chunk (j0 + jt) * 8 + lane, 4 tiles at a time
+    if (warp == kProducerWarp) {
         if (lane == 0) {
             mbar_init(&bars[BQ], 1);
             for (int st = 0; st < kStagesK; ++st) {
@@ -200,8 +207,18 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             *abort_flag = 0;
             fence_mbar_init();
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(&bars[BQ], GM::kQBytes);
+#pragma unroll
+            for (int h = 0; h < GM::kHalves; ++h)
+                tma_load_3d(smem + GM::kOffQ + h * kHalf, &tm_q, 64 * h, kvh * G, qrow0,
+                            &bars[BQ]);
         }
-        __syncwarp();
+        const int i = j0 * (kKeys / kChunk) + lane;
+        ids = (i < nchunks) ? __ldg(bt + (i >> csh)) : 0;
+    } else if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
@@ -220,25 +237,11 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         // chunk (32 chunks = 4 KV tiles per refill, independent loads), lane 0 sets the
         // byte counts and lane b < 8 issues the box of chunk b of the tile.  A chunk is
         // a whole block (block size 16) or rows 16 h .. 16 h + 15 of one (block size 32).
-        const int32_t* bt =
-            a.block_tables + static_cast<size_t>(cascade ? 0 : r) * a.max_blocks_per_seq;
-        const int nchunks = max_lim / kChunk + 1;
-        const int csh = a.block_size == 32 ? 1 : 0;   // log2 of chunks per block
-        if (lane == 0) {
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(&bars[BQ], GM::kQBytes);
-#pragma unroll
-            for (int h = 0; h < GM::kHalves; ++h)
-                tma_load_3d(smem + GM::kOffQ + h * kHalf, &tm_q, 64 * h, kvh * G, qrow0,
-                            &bars[BQ]);
-        }
-        int ids = 0;
+        // The Q copy and the first block ids were started before the CTA-wide barrier.
         int k_issued = 0, v_issued = 0;   // tiles whose K / V copies were issued
         for (int jt = 0; jt < ntiles; ++jt) {
             constexpr int kPerTile = kKeys / kChunk;   // 8 chunks per KV tile
-            if ((jt & 3) == 0) {
+            if ((jt & 3) == 0 && jt > 0) {
                 const int i = (j0 + jt) * kPerTile + lane;
                 ids = (i < nchunks) ? __ldg(bt + (i >> csh)) : 0;
             }
@@ -534,19 +537,28 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 a.m_part[prow] = m;   // log2 domain, as the decode partials
                 a.l_part[prow] = lsum;
             }
+            // 64 columns of both accumulators per TMEM round trip
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                float o[32];
-                tmem_ld32(tmem + lane_addr + kTmemO + q * 32, o);
-                tmem_wait_ld();
+            for (int q2 = 0; q2 < D / 64; ++q2) {
+            float oo[2][32], o1[2][32];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                tmem_ld32(tmem + lane_addr + kTmemO + (2 * q2 + hh) * 32, oo[hh]);
+            if (n1 > 0) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    tmem_ld32(tmem + lane_addr + kTmemO + 128 + (2 * q2 + hh) * 32, o1[hh]);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int q = 2 * q2 + hh;
+                float* o = oo[hh];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] *= c0;
                 if (n1 > 0) {
-                    float o1[32];
-                    tmem_ld32(tmem + lane_addr + kTmemO + 128 + q * 32, o1);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = fmaf(o1[e], c1, o[e]);
+                    for (int e = 0; e < 32; ++e) o[e] = fmaf(o1[hh][e], c1, o[e]);
                 }
                 if (cascade && row_valid) {
                     float* dst = a.o_part + prow * D + q * 32;
@@ -565,6 +577,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                         *reinterpret_cast<uint4*>(orow + q * 32 + e) = w;
                     }
                 }
+            }
             }
         }
     }

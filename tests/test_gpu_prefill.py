@@ -113,3 +113,17 @@ def test_prefix_cached_prefill_published_config_sampled(pkv, oracle_mod):
     out = run_prefill(pkv, case)
     check_attention(out, ref, mask=want)
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_prefill_out_of_range_block_id_raises_status(pkv, dtype):
+    """A table entry past the pool inside a request's keys is not read (the tcgen05
+    kernel stages block 0 in its place, the fp32 kernel zeros), and is reported."""
+    case = custom_case(32, 8, [100, 40], [37, 64], seed=11, num_blocks=64, dtype=dtype)
+    bt = case.block_tables.clone()
+    bt[0, 2] = 64          # one past the last block: keys 32..47 of request 0
+    pkv.paged_prefill(case.q, case.k_pool, case.v_pool, bt, case.cached_lens, case.new_lens,
+                      case.q_offsets, case.scale, max_new=int(case.new_lens.max()))
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 5
+    assert pkv.read_device_status() == 0
