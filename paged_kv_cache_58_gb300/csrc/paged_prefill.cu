@@ -44,7 +44,17 @@
 // halves x 8 rows x 128 B, 128-byte swizzle), so a K/V tile lands as [8-key group]
 // [column half][8 rows][128 B]: a valid K-major operand (8-row atoms 2 KB apart) for S
 // and MN-major operand (column halves 1 KB apart) for P.V; at head_dim 64 a 16-row x
-// 64-column box, the tile one 64-column half with 8-row atoms 1 KB apart.
+// 64-column box, the tile one 64-column half with 8-row atoms 1 KB apart.  On the
+// tile holding the last key a query tile needs, the P.V product skips the 16-key steps
+// wholly past that key (P = 0 there), and the issuer zeroes the V rows of its last step
+// past it (they may hold NaN from unused slots) once V has landed.
+//
+// Persistent CTAs.  A CTA pays about 5 us outside its tile loop (barrier and TMEM set-up,
+// the first gathers and S, the epilogue), which nothing overlaps when each SM runs one
+// CTA; with at most 128 requests (and outside cascade mode) the grid is one CTA per SM
+// and each works through a share of the query tiles (the work items below), with the
+// next item's Q, gathers and first S products under way while the softmax warps finish
+// the current one.
 //
 // Measured costs per 128-key tile on GB300 (clock64 traces and isolated probes): the
 // 24 N = 128 MMAs (8 for S, 16 for the hi + lo P.V) take the tensor pipe about 1700
@@ -76,7 +86,9 @@ constexpr int kChunk = 16;                 // tokens per staged chunk: a block, 
 constexpr int kHalf = kRows * 128;         // one 64-column half of the 128-row Q tile: 16 KB
 constexpr int kStagesK = 3;                // K stages: freed right after S = Q K^T
 constexpr int kStagesV = 3;                // V stages: freed after P.V
-constexpr int kNumBars = 21;
+constexpr int kNumBars = 24;
+
+constexpr int kMaxSchedReqs = 128;   // persistent scheduling ranks up to 128 requests
 
 // Shared-memory geometry for head_dim D (64 or 128).
 template <int D>
@@ -90,7 +102,10 @@ struct Geom {
     static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
     static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
-    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
+    // barriers, then the TMEM address and abort flag, then the persistent schedule
+    static constexpr int kOffSreq = kOffBar + kNumBars * 8 + 16;
+    static constexpr int kOffOff = kOffSreq + kMaxSchedReqs * 2;
+    static constexpr int kSmemBytes = kOffOff + (kMaxSchedReqs + 1) * 4 + 1024;  // + align slack
 };
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
@@ -102,8 +117,11 @@ constexpr float kLazyRescale = 8.0f;       // log2 units
 constexpr float kNoMax = -1.0e30f;         // running max before a stream saw a key
 
 // barrier indices: K/V stages (tile j uses stage j % 3), per-stream S/P buffer state.
+// BQ_EMPTY: every S of an item has run (the Q buffer may be reloaded); BO_FREE: per
+// stream, the softmax warps have read that stream's O out for an item.
 constexpr int BQ = 0, BK_FULL = 1, BK_EMPTY = 4, BV_FULL = 7, BV_EMPTY = 10, BS_FULL = 13,
-              BP_FULL = 15, BPV_DONE = 17, BDRAIN = 19;   // BDRAIN: per stream, at exit
+              BP_FULL = 15, BPV_DONE = 17, BDRAIN = 19,   // BDRAIN: per stream, at exit
+              BQ_EMPTY = 21, BO_FREE = 22;
 
 struct Ctl {
     uint64_t* bars;
@@ -134,11 +152,99 @@ PKV_DEVINL bool wait_bar_warp(const Ctl& c, int idx, uint32_t parity, int lane) 
     }
 }
 
+// ------------------------------------------------------------------ work items
+// An item is one 128-row query tile of one request and kv head.  With `persistent`
+// set the grid holds at most one CTA per SM, and CTA b works through the items k =
+// m P + (b, or P - 1 - b for odd m), m = 0, 1, ... (P CTAs, a snake over the item list)
+// of a list that ranks the requests by their key count, longest first, and within a
+// request takes the query tiles last-first: the longest items are spread over the CTAs
+// first and each CTA's total comes out near the mean.  Each role walks the same list, so
+// barrier phases carry over from one item to the next and the next item's gathers and
+// first S products start while the softmax warps finish the current one.  Otherwise
+// CTA (x, y, z) takes the single item (query tile x, kv head y, request z -- in
+// cascade mode split z).
+
+struct ItemParams {
+    int kvh, r, n, c, t0, max_lim, j0, ntiles, qoff, qrow0;
+    bool p_single;
+};
+
+// Parameters of item (qt, kvh, r); false when it has no rows (t0 >= n), no tile, or
+// keys past its table (then PKV_ERR_OOB is raised when `report`).
+template <int G>
+PKV_DEVINL bool item_params(const PrefillArgs& a, int qt, int kvh, int r, bool report,
+                            ItemParams& p) {
+    constexpr int TOK = kRows / G;
+    const bool cascade = a.cascade != 0;   // rows = sequences over the c shared keys
+    p.kvh = kvh;
+    p.r = r;
+    p.n = cascade ? a.cascade_rows : __ldg(a.new_lens + r);
+    p.c = cascade ? a.cascade_keys : __ldg(a.cached_lens + r);
+    p.t0 = qt * TOK;
+    if (p.t0 >= p.n) return false;
+    const int L = cascade ? p.c : p.c + p.n;   // keys in the pool for this request
+    if (p.c < 0 || L <= 0 || L > a.max_blocks_per_seq * a.block_size) {
+        if (report) raise_status(a.status, PKV_ERR_OOB);
+        return false;
+    }
+    const int i_last = min(p.t0 + TOK, p.n) - 1;
+    p.max_lim = cascade ? p.c - 1 : p.c + i_last;   // last key any row of the tile sees
+    // KV tiles [j0, j0 + ntiles): all of them, or in cascade mode the range of split r
+    // (its partial goes to slot r; the host sizes the splits so that none is empty).
+    p.j0 = cascade ? r * a.cascade_tiles_per_split : 0;
+    p.ntiles = cascade ? min(p.max_lim / kKeys + 1 - p.j0, a.cascade_tiles_per_split)
+                       : p.max_lim / kKeys + 1;
+    if (p.ntiles <= 0) return false;
+    p.qoff = cascade ? 0 : __ldg(a.q_offsets + r);
+    p.qrow0 = p.qoff + p.t0;   // first token row of the tile in q / out
+    // Every row of the tile attends at least min_keys keys (its first token the fewest).
+    const int min_keys = cascade ? p.c : p.c + p.t0 + 1;
+    p.p_single = min_keys >= a.p_single_min_keys;
+    return true;
+}
+
+struct Sched {
+    const uint16_t* sreq;   // persistent: requests by rank (most keys first)
+    const int* off;         // persistent: off[rho] = first item of rank rho; off[R] = items
+    int R;
+    bool persistent;
+};
+
+struct Cursor {
+    int m = 0;     // the CTA's items visited
+    int rho = 0;   // rank of the request holding the last one
+};
+
+// The CTA's next item; false when it has none left.
+template <int G>
+PKV_DEVINL bool next_item(const PrefillArgs& a, const Sched& s, Cursor& cur, bool report,
+                          ItemParams& p) {
+    if (!s.persistent) {
+        if (cur.m++ > 0) return false;
+        return item_params<G>(a, blockIdx.x, blockIdx.y, blockIdx.z, report, p);
+    }
+    const int P = gridDim.x;
+    const int b = blockIdx.x;
+    const int total = s.off[s.R];
+    for (;;) {
+        const int m = cur.m++;
+        const int k = m * P + ((m & 1) ? P - 1 - b : b);
+        if (k >= total) return false;
+        while (s.off[cur.rho + 1] <= k) ++cur.rho;   // k grows with m
+        const int rem = k - s.off[cur.rho];
+        const int nq = (s.off[cur.rho + 1] - s.off[cur.rho]) / a.num_kv_heads;
+        if (item_params<G>(a, nq - 1 - rem / a.num_kv_heads, rem % a.num_kv_heads,
+                           s.sreq[cur.rho], report, p))
+            return true;
+    }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+                       const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a,
+                       const int persistent) {
     using GM = Geom<D>;
     constexpr int TOK = kRows / G;
     extern __shared__ uint8_t smem_raw[];
@@ -147,52 +253,73 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     griddep_wait();
     griddep_launch_dependents();
-    const int qt = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int r = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    const bool cascade = a.cascade != 0;    // rows = sequences over the c shared keys
-    const int n = cascade ? a.cascade_rows : a.new_lens[r];
-    const int c = cascade ? a.cascade_keys : a.cached_lens[r];
-    const int t0 = qt * TOK;
-    if (t0 >= n) return;  // uniform over the CTA, before any barrier or TMEM use
-    const int L = cascade ? c : c + n;       // keys in the pool for this request
-    if (c < 0 || L <= 0 || L > a.max_blocks_per_seq * a.block_size) {
-        if (threadIdx.x == 0) raise_status(a.status, PKV_ERR_OOB);
-        return;
-    }
-    const int i_last = min(t0 + TOK, n) - 1;
-    const int max_lim = cascade ? c - 1 : c + i_last;   // last key any row of this tile sees
-    // KV tiles [j0, j0 + ntiles) of this CTA: all of them, or in cascade mode the range
-    // of split blockIdx.z (its partial goes to slot blockIdx.z; the host sizes the
-    // splits so that none is empty).
-    const int j0 = cascade ? r * a.cascade_tiles_per_split : 0;
-    const int ntiles =
-        cascade ? min(max_lim / kKeys + 1 - j0, a.cascade_tiles_per_split) : max_lim / kKeys + 1;
-    if (ntiles <= 0) return;   // uniform over the CTA, before any barrier or TMEM use
-    const int qoff = cascade ? 0 : a.q_offsets[r];
-    const int qrow0 = qoff + t0;             // first token row of the tile in q / out
-    // Every row of the tile attends at least min_keys keys (its first token the fewest).
-    const int min_keys = cascade ? c : c + t0 + 1;
-    const bool p_single = min_keys >= a.p_single_min_keys;   // uniform over the CTA
+    const bool cascade = a.cascade != 0;
+    const int csh = a.block_size == 32 ? 1 : 0;   // log2 of chunks per block
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GM::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + GM::kOffBar + kNumBars * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint16_t* sreq = reinterpret_cast<uint16_t*>(smem + GM::kOffSreq);
+    int* off = reinterpret_cast<int*>(smem + GM::kOffOff);
     Ctl ctl{bars, abort_flag, a.status};
+    const Sched sch{sreq, off, a.num_reqs, persistent != 0};
 
-    // The producer warp sets up the barriers and starts the Q copy and the block-id loads
-    // of the first KV tiles before the CTA-wide barrier, beside the TMEM allocation.
-    const int32_t* bt =
-        a.block_tables + static_cast<size_t>(cascade ? 0 : r) * a.max_blocks_per_seq;
-    const int nchunks = max_lim / kChunk + 1;
-    const int csh = a.block_size == 32 ? 1 : 0;   // log2 of chunks per block
-    int ids = 0;   // producer: block id of chunk (j0 + jt) * 8 + lane, 4 tiles at a time
+    if (sch.persistent) {
+        // Rank the requests by key count (most first, ties by index) and lay out the
+        // item list: rank rho holds ceil(n / TOK) query tiles x the kv heads.
+        const int R = a.num_reqs;
+        for (int t = threadIdx.x; t < R; t += kThreads)   // off[] holds the key counts first
+            off[t] = __ldg(a.cached_lens + t) + __ldg(a.new_lens + t);
+        __syncthreads();
+        for (int t = threadIdx.x; t < R; t += kThreads) {
+            const int kt = off[t];
+            int rank = 0;
+            for (int u = 0; u < R; ++u) {
+                const int ku = off[u];
+                rank += (ku > kt) || (ku == kt && u < t);
+            }
+            sreq[rank] = static_cast<uint16_t>(t);
+        }
+        __syncthreads();
+        if (warp == 0) {   // exclusive scan of the item counts over the ranks, 4 per lane
+            int cnt[4], sum = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int rho = lane * 4 + e;
+                int v = 0;
+                if (rho < R) {
+                    const int nn = __ldg(a.new_lens + sreq[rho]);
+                    v = nn > 0 ? (nn + TOK - 1) / TOK * a.num_kv_heads : 0;
+                }
+                cnt[e] = v;
+                sum += v;
+            }
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            int run = incl - sum;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int rho = lane * 4 + e;
+                if (rho < R) off[rho] = run;
+                run += cnt[e];
+                if (rho == R - 1) off[R] = run;
+            }
+        }
+        __syncthreads();
+    }
+
     if (warp == kProducerWarp) {
         if (lane == 0) {
             mbar_init(&bars[BQ], 1);
+            mbar_init(&bars[BQ_EMPTY], 2);
+            mbar_init(&bars[BO_FREE + 0], kSoftmaxWarps);
+            mbar_init(&bars[BO_FREE + 1], kSoftmaxWarps);
             for (int st = 0; st < kStagesK; ++st) {
                 mbar_init(&bars[BK_FULL + st], 1);
                 mbar_init(&bars[BK_EMPTY + st], 1);
@@ -210,14 +337,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(&bars[BQ], GM::kQBytes);
-#pragma unroll
-            for (int h = 0; h < GM::kHalves; ++h)
-                tma_load_3d(smem + GM::kOffQ + h * kHalf, &tm_q, 64 * h, kvh * G, qrow0,
-                            &bars[BQ]);
         }
-        const int i = j0 * (kKeys / kChunk) + lane;
-        ids = (i < nchunks) ? __ldg(bt + (i >> csh)) : 0;
     } else if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -237,58 +357,82 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         // chunk (32 chunks = 4 KV tiles per refill, independent loads), lane 0 sets the
         // byte counts and lane b < 8 issues the box of chunk b of the tile.  A chunk is
         // a whole block (block size 16) or rows 16 h .. 16 h + 15 of one (block size 32).
-        // The Q copy and the first block ids were started before the CTA-wide barrier.
+        // Stages and their phases count the CTA's tiles over all its items (g); the Q of
+        // an item is loaded once every S product of the previous item has run.
+        Cursor cur;
+        ItemParams p;
+        int it = 0, g = 0;
         int k_issued = 0, v_issued = 0;   // tiles whose K / V copies were issued
-        for (int jt = 0; jt < ntiles; ++jt) {
-            constexpr int kPerTile = kKeys / kChunk;   // 8 chunks per KV tile
-            if ((jt & 3) == 0 && jt > 0) {
-                const int i = (j0 + jt) * kPerTile + lane;
-                ids = (i < nchunks) ? __ldg(bt + (i >> csh)) : 0;
+        bool ok = true;
+        while (ok && next_item<G>(a, sch, cur, lane == 0, p)) {
+            const int32_t* bt =
+                a.block_tables + static_cast<size_t>(cascade ? 0 : p.r) * a.max_blocks_per_seq;
+            const int nchunks = p.max_lim / kChunk + 1;
+            if (it >= 1 && !wait_bar_warp(ctl, BQ_EMPTY, (it - 1) & 1, lane)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[BQ], GM::kQBytes);
+#pragma unroll
+                for (int h = 0; h < GM::kHalves; ++h)
+                    tma_load_3d(smem + GM::kOffQ + h * kHalf, &tm_q, 64 * h, p.kvh * G, p.qrow0,
+                                &bars[BQ]);
             }
-            const int sk = jt % kStagesK;
-            const int sv = jt % kStagesV;
-            const int nb = min(kPerTile, nchunks - (j0 + jt) * kPerTile);
-            int phys = __shfl_sync(0xffffffffu, ids, ((jt & 3) * kPerTile) + (lane & 7));
-            if (phys < 0 || phys >= a.num_blocks) {
-                if (lane < nb) raise_status(a.status, PKV_ERR_OOB);
-                phys = 0;  // keep the byte count; the output is flagged invalid
+            ++it;
+            int ids = 0;
+            for (int jt = 0; jt < p.ntiles; ++jt, ++g) {
+                constexpr int kPerTile = kKeys / kChunk;   // 8 chunks per KV tile
+                if ((jt & 3) == 0) {
+                    const int i = (p.j0 + jt) * kPerTile + lane;
+                    ids = (i < nchunks) ? __ldg(bt + (i >> csh)) : 0;
+                }
+                const int sk = g % kStagesK;
+                const int sv = g % kStagesV;
+                const int nb = min(kPerTile, nchunks - (p.j0 + jt) * kPerTile);
+                int phys = __shfl_sync(0xffffffffu, ids, ((jt & 3) * kPerTile) + (lane & 7));
+                if (phys < 0 || phys >= a.num_blocks) {
+                    if (lane < nb) raise_status(a.status, PKV_ERR_OOB);
+                    phys = 0;  // keep the byte count; the output is flagged invalid
+                }
+                const int chunk = (p.j0 + jt) * kPerTile + (lane & 7);
+                const int row = (phys * a.num_kv_heads + p.kvh) * a.block_size +
+                                (chunk & ((1 << csh) - 1)) * kChunk;
+                // K of tile g: its stage is free once S of tile g - kStagesK has run.  The
+                // warp stays converged: lane 0 sets the byte count and lanes b < nb issue
+                // the boxes through predicated instructions.
+                if (g >= kStagesK &&
+                    !wait_bar_warp(ctl, BK_EMPTY + sk, ((g / kStagesK) - 1) & 1, lane)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx_if(lane == 0, &bars[BK_FULL + sk], nb * GM::kChunkBytes);
+                {
+                    uint8_t* dst = smem + GM::kOffK + sk * GM::kTileBytes + lane * GM::kChunkBytes;
+                    if constexpr (D == 128)
+                        tma_load_4d_if(lane < nb, dst, &tm_k, 0, 0, 0, row / 8, &bars[BK_FULL + sk]);
+                    else
+                        tma_load_2d_if(lane < nb, dst, &tm_k, 0, row, &bars[BK_FULL + sk]);
+                }
+                ++k_issued;
+                // V of tile g: its stage is free once P.V of tile g - kStagesV has run.
+                if (g >= kStagesV &&
+                    !wait_bar_warp(ctl, BV_EMPTY + sv, ((g / kStagesV) - 1) & 1, lane)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx_if(lane == 0, &bars[BV_FULL + sv], nb * GM::kChunkBytes);
+                {
+                    uint8_t* dst = smem + GM::kOffV + sv * GM::kTileBytes + lane * GM::kChunkBytes;
+                    if constexpr (D == 128)
+                        tma_load_4d_if(lane < nb, dst, &tm_v, 0, 0, 0, row / 8, &bars[BV_FULL + sv]);
+                    else
+                        tma_load_2d_if(lane < nb, dst, &tm_v, 0, row, &bars[BV_FULL + sv]);
+                }
+                ++v_issued;
             }
-            const int chunk = (j0 + jt) * kPerTile + (lane & 7);
-            const int row = (phys * a.num_kv_heads + kvh) * a.block_size +
-                            (chunk & ((1 << csh) - 1)) * kChunk;
-            // K of tile jt: its stage is free once S of tile jt - kStagesK has run.  The
-            // warp stays converged: lane 0 sets the byte count and lanes b < nb issue the
-            // boxes through predicated instructions.
-            if (jt >= kStagesK &&
-                !wait_bar_warp(ctl, BK_EMPTY + sk, ((jt / kStagesK) - 1) & 1, lane))
-                break;
-            mbar_arrive_expect_tx_if(lane == 0, &bars[BK_FULL + sk], nb * GM::kChunkBytes);
-            {
-                uint8_t* dst = smem + GM::kOffK + sk * GM::kTileBytes + lane * GM::kChunkBytes;
-                if constexpr (D == 128)
-                    tma_load_4d_if(lane < nb, dst, &tm_k, 0, 0, 0, row / 8, &bars[BK_FULL + sk]);
-                else
-                    tma_load_2d_if(lane < nb, dst, &tm_k, 0, row, &bars[BK_FULL + sk]);
-            }
-            ++k_issued;
-            // V of tile jt: its stage is free once P.V of tile jt - kStagesV has run.
-            if (jt >= kStagesV &&
-                !wait_bar_warp(ctl, BV_EMPTY + sv, ((jt / kStagesV) - 1) & 1, lane))
-                break;
-            mbar_arrive_expect_tx_if(lane == 0, &bars[BV_FULL + sv], nb * GM::kChunkBytes);
-            {
-                uint8_t* dst = smem + GM::kOffV + sv * GM::kTileBytes + lane * GM::kChunkBytes;
-                if constexpr (D == 128)
-                    tma_load_4d_if(lane < nb, dst, &tm_v, 0, 0, 0, row / 8, &bars[BV_FULL + sv]);
-                else
-                    tma_load_2d_if(lane < nb, dst, &tm_v, 0, row, &bars[BV_FULL + sv]);
-            }
-            ++v_issued;
         }
         // Drain (also after an abort): wait, bounded, until the last copy issued into
         // every stage has landed, so that no TMA write into shared memory outlives the
         // CTA.  No later copy goes into those stages, so the phases cannot move on.
-        mbar_wait_warp(&bars[BQ], 0, a.status);
+        if (it >= 1) mbar_wait_warp(&bars[BQ], (it - 1) & 1, a.status);
         for (int st = 0; st < kStagesK; ++st) {
             if (k_issued > st) {
                 const int last = st + kStagesK * ((k_issued - 1 - st) / kStagesK);
@@ -301,14 +445,20 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
         // ------------------------------------------------------------ MMA issuers
-        // Stream sm = warp - kMmaWarp owns KV tiles j = sm, sm + 2, ...: S_j into its
-        // S/P buffer, then O_sm += P_j V_j once the softmax has written P_j there, then
+        // Stream sm = warp - kMmaWarp owns an item's KV tiles j = sm, sm + 2, ...: S_j into
+        // its S/P buffer, then O_sm += P_j V_j once the softmax has written P_j there, then
         // S_{j+2} into the same buffer once that P.V has completed.  Each stream is a
         // serial chain, but the two interleave in the tensor pipe.  Each issuing warp
         // shares its scheduler with a softmax warp and gets only the issue slots that
         // warp leaves free, so the loop is short: the whole warp runs it converged (all
         // lanes poll, then one leader lane issues through predicated instructions), and
-        // the descriptors are precomputed halves plus constant offsets.
+        // the descriptors are precomputed halves plus constant offsets.  Across items:
+        // an item's first P.V into O_sm waits until the softmax warps have read O_sm out
+        // for the last item in which this stream had tiles (BO_FREE + sm, one phase per
+        // such item), and once this stream's last S of an item has run it signals that
+        // the Q buffer may take the next item's Q (BQ_EMPTY; a stream without tiles in
+        // the item just arrives).  Both issuers wait for every phase of BQ, tiles or not,
+        // so that no parity wait can fall two phases behind.
         constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, kKeys, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, D, false, true);
         constexpr uint32_t hi_q = smem_desc_sw128_hi(1024);          // Q: 8-row atoms 1 KB apart
@@ -320,43 +470,98 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         const uint32_t tS = tmem + sm * 128;
         const uint32_t tO = tmem + kTmemO + sm * 128;
         const bool leader = elect_one();   // issues every MMA and commit of this stream
-        bool ok = wait_bar_warp(ctl, BQ, 0, lane);
-        for (int j = sm; ok && j < ntiles; j += 2) {
-            const int st = j % kStagesK;
-            const uint32_t use = static_cast<uint32_t>(j >> 1);   // this stream's tile count
-            // S_j: K_j landed, and P_{j-2} in the buffer consumed by its P.V.
-            if (!wait_bar_warp(ctl, BK_FULL + st, (j / kStagesK) & 1, lane)) break;
-            if (j >= 2 && !wait_bar_warp(ctl, BPV_DONE + sm, (use - 1) & 1, lane)) break;
-            tc_fence_after();
-            {
-                const uint32_t lk = lo_k + ((st * GM::kTileBytes) >> 4);
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t kc = ((ks & 3) * 32) >> 4;   // 16 columns = 32 B
-                    umma_bf16_if(leader, tS,
-                                 desc_join(lo_q + (((ks >> 2) * kHalf) >> 4) + kc, hi_q),
-                                 desc_join(lk + (((ks >> 2) * 1024) >> 4) + kc, hi_kv), idesc_qk,
-                                 ks > 0);
+        Cursor cur;
+        ItemParams p;
+        int it = 0, g0 = 0;
+        uint32_t use = 0;     // this stream's tiles over all items (S/P buffer phases)
+        uint32_t o_use = 0;   // items in which this stream had tiles (O_sm read-outs)
+        bool ok = true;
+        while (ok && next_item<G>(a, sch, cur, false, p)) {
+            ok = wait_bar_warp(ctl, BQ, it & 1, lane);
+            bool o_free = o_use == 0;   // O_sm read out after its last item
+            for (int j = sm; ok && j < p.ntiles; j += 2, ++use) {
+                const int g = g0 + j;
+                const int st = g % kStagesK;
+                // S_j: K_j landed, and P of this buffer's previous tile consumed by its P.V.
+                if (!wait_bar_warp(ctl, BK_FULL + st, (g / kStagesK) & 1, lane)) { ok = false; break; }
+                if (use >= 1 && !wait_bar_warp(ctl, BPV_DONE + sm, (use - 1) & 1, lane)) {
+                    ok = false;
+                    break;
                 }
-                umma_commit_if(leader, &bars[BS_FULL + sm]);
-                umma_commit_if(leader, &bars[BK_EMPTY + st]);
-            }
-            // O_sm += P_j V_j: P_j written, V_j landed.
-            if (!wait_bar_warp(ctl, BP_FULL + sm, use & 1, lane)) break;
-            if (!wait_bar_warp(ctl, BV_FULL + st, (j / kStagesV) & 1, lane)) break;
-            tc_fence_after();
-            {
-                const uint32_t lv = lo_v + ((st * GM::kTileBytes) >> 4);
-                // V as the MN-major B operand: 16 keys = two 8-key groups.
+                tc_fence_after();
+                {
+                    const uint32_t lk = lo_k + ((st * GM::kTileBytes) >> 4);
 #pragma unroll
-                for (int ks = 0; ks < kKeys / 16; ++ks) {
-                    const uint64_t bv = desc_join(lv + ((ks * 2 * GM::kGroupBytes) >> 4), hi_kv);
-                    umma_bf16_ta_if(leader, tO, tS + ks * 8, bv, idesc_pv, (j >= 2) || (ks > 0));
-                    if (!p_single) umma_bf16_ta_if(leader, tO, tS + 64 + ks * 8, bv, idesc_pv, true);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t kc = ((ks & 3) * 32) >> 4;   // 16 columns = 32 B
+                        umma_bf16_if(leader, tS,
+                                     desc_join(lo_q + (((ks >> 2) * kHalf) >> 4) + kc, hi_q),
+                                     desc_join(lk + (((ks >> 2) * 1024) >> 4) + kc, hi_kv),
+                                     idesc_qk, ks > 0);
+                    }
+                    umma_commit_if(leader, &bars[BS_FULL + sm]);
+                    umma_commit_if(leader, &bars[BK_EMPTY + st]);
+                    if (j + 2 >= p.ntiles) umma_commit_if(leader, &bars[BQ_EMPTY]);   // last S
                 }
-                umma_commit_if(leader, &bars[BPV_DONE + sm]);
-                umma_commit_if(leader, &bars[BV_EMPTY + st]);
+                // O_sm += P_j V_j: P_j written, V_j landed, O_sm read out (first tile).
+                const int sv = g % kStagesV;
+                if (!wait_bar_warp(ctl, BP_FULL + sm, use & 1, lane)) { ok = false; break; }
+                if (!wait_bar_warp(ctl, BV_FULL + sv, (g / kStagesV) & 1, lane)) { ok = false; break; }
+                if (!o_free) {
+                    if (!wait_bar_warp(ctl, BO_FREE + sm, (o_use - 1) & 1, lane)) {
+                        ok = false;
+                        break;
+                    }
+                    o_free = true;
+                }
+                // Keys past the last one this tile needs are masked for every row (P = 0),
+                // but their V rows may hold anything (NaN in unused slots, stale data where
+                // no block was loaded this tile).  The P.V product skips the 16-key steps
+                // that lie wholly past that key, and the rows of the last step past it are
+                // zeroed, now that V_j has landed, so that 0 * V stays 0.
+                const int kbase = (p.j0 + j) * kKeys;
+                const int nvalid = min(kKeys, p.max_lim - kbase + 1);   // >= 1
+                const int ksteps = (nvalid + 15) >> 4;
+                if (nvalid < ksteps * 16) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    // rows nvalid .. 16 ksteps - 1, 8 pieces per 128-byte half: lane = piece
+                    // 8 rows apart so that each store instruction touches 8 rows of an atom
+                    const int rows = ksteps * 16 - nvalid;
+                    for (int t = lane; t < rows * 8 * GM::kHalves; t += 32) {
+                        const int row = nvalid + t / (8 * GM::kHalves);
+                        const int hh = (t / 8) % GM::kHalves;
+                        const int jj = t & 7;
+                        uint8_t* vrow = smem + GM::kOffV + sv * GM::kTileBytes +
+                                        (row >> 3) * GM::kGroupBytes + (row & 7) * 128;
+                        *reinterpret_cast<uint4*>(vrow + hh * 1024 + ((jj ^ (row & 7)) << 4)) = z;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                tc_fence_after();
+                {
+                    const uint32_t lv = lo_v + ((sv * GM::kTileBytes) >> 4);
+                    // V as the MN-major B operand: 16 keys = two 8-key groups.
+#pragma unroll
+                    for (int ks = 0; ks < kKeys / 16; ++ks) {
+                        const uint64_t bv = desc_join(lv + ((ks * 2 * GM::kGroupBytes) >> 4), hi_kv);
+                        umma_bf16_ta_if(leader && ks < ksteps, tO, tS + ks * 8, bv, idesc_pv,
+                                        (j >= 2) || (ks > 0));
+                        if (!p.p_single)
+                            umma_bf16_ta_if(leader && ks < ksteps, tO, tS + 64 + ks * 8, bv,
+                                            idesc_pv, true);
+                    }
+                    umma_commit_if(leader, &bars[BPV_DONE + sm]);
+                    umma_commit_if(leader, &bars[BV_EMPTY + sv]);
+                }
             }
+            if (!ok) break;
+            if (sm >= p.ntiles)
+                mbar_arrive_if(leader, &bars[BQ_EMPTY]);   // no S in this item
+            else
+                ++o_use;
+            g0 += p.ntiles;
+            ++it;
         }
         // Drain (also after an abort): every MMA this stream issued completes before
         // the TMEM is freed at the end of the kernel.
@@ -366,20 +571,28 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         // ------------------------------------------------------------ softmax + epilogue
         const int row = threadIdx.x;              // 0..127 == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-        const int tok = t0 + row / G;
-        const int head = kvh * G + row % G;
-        const bool row_valid = tok < n;
-        const int lim = cascade ? c - 1 : (row_valid ? c + tok : c + n - 1);  // last key seen
         const float sl2 = a.scale_log2;
+        Cursor cur;
+        ItemParams p;
+        int g0 = 0;                  // the CTA's KV tiles before this item
+        uint32_t use0 = 0, use1 = 0;   // tiles of each stream over all items
+        bool ok = true;
+        while (ok && next_item<G>(a, sch, cur, false, p)) {
+        const int tok = p.t0 + row / G;
+        const int head = p.kvh * G + row % G;
+        const bool row_valid = tok < p.n;
+        const int lim = cascade ? p.c - 1 : (row_valid ? p.c + tok : p.c + p.n - 1);  // last key seen
+        const bool p_single = p.p_single;
+        const int ntiles = p.ntiles;
         // Running max (log2 domain) and row sum of each stream: even and odd KV tiles
         // accumulate into separate O buffers and are merged after the last tile.
         float m_st[2] = {kNoMax, kNoMax};
         float l_st[2] = {0.f, 0.f};
-        bool ok = true;
         for (int jt = 0; jt < ntiles; ++jt) {
             const int sm = jt & 1;
+            const uint32_t us = sm ? use1 : use0;   // this tile's use of the stream's buffers
             const uint32_t tS = tmem + lane_addr + sm * 128;
-            if (!wait_bar_warp(ctl, BS_FULL + sm, (jt >> 1) & 1, lane)) { ok = false; break; }
+            if (!wait_bar_warp(ctl, BS_FULL + sm, us & 1, lane)) { ok = false; break; }
             tc_fence_after();
             float x[kKeys];
 #pragma unroll
@@ -387,7 +600,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tmem_ld32(tS + q * 32, *reinterpret_cast<float(*)[32]>(&x[q * 32]));
             tmem_wait_ld();
 
-            const int kbase = (j0 + jt) * kKeys;
+            const int kbase = (p.j0 + jt) * kKeys;
             if (kbase + kKeys - 1 > lim) {
 #pragma unroll
                 for (int k = 0; k < kKeys; ++k) x[k] = (kbase + k <= lim) ? x[k] : -INFINITY;
@@ -413,7 +626,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             // previous P.V (tile jt - 2) has completed already: S_jt waited for it before
             // overwriting the buffer; the wait below only makes that visible here.
             if (jt >= 2 && __any_sync(0xffffffffu, grow)) {
-                if (!wait_bar_warp(ctl, BPV_DONE + sm, ((jt >> 1) - 1) & 1, lane)) {
+                if (!wait_bar_warp(ctl, BPV_DONE + sm, (us - 1) & 1, lane)) {
                     ok = false;
                     break;
                 }
@@ -489,40 +702,21 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 m_st[0] = m_cur;
             }
             tmem_wait_st();
-            // Keys past the last one this tile needs are masked for every row, but their
-            // V rows may hold anything (NaN in unused slots, stale data where no block was
-            // loaded this tile); zero them so that 0 * V stays 0 in the P.V product, once
-            // this tile's V has landed.
-            if (kbase + kKeys - 1 > max_lim) {
-                if (!wait_bar_warp(ctl, BV_FULL + jt % kStagesV, (jt / kStagesV) & 1, lane)) {
-                    ok = false;
-                    break;
-                }
-                if (kbase + row > max_lim) {
-                    uint8_t* vrow = smem + GM::kOffV + (jt % kStagesV) * GM::kTileBytes +
-                                    (row >> 3) * GM::kGroupBytes + (row & 7) * 128;
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-                    // the whole 128-byte row, its 16-byte pieces in rotated order so that
-                    // the 8 rows of an atom hit 8 different bank groups at each step
-#pragma unroll
-                    for (int h = 0; h < GM::kHalves; ++h)
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<uint4*>(vrow + h * 1024 + ((j ^ (row & 7)) << 4)) = z;
-                }
-                fence_proxy_async_smem();
-            }
             tc_fence_before();
             __syncwarp();
             mbar_arrive_if(lane == 0, &bars[BP_FULL + sm]);
+            if (sm) ++use1; else ++use0;
         }
+        if (!ok) break;
         // ------------------------------------------------------------ epilogue
         // Merge the streams: with a_s = 2^(m_s - m), m = max(m_0, m_1),
         //   O = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1).
         // Stream 0 always holds key 0, which every row sees, so m_0 and l_0 are proper.
         const int n0 = (ntiles + 1) >> 1, n1 = ntiles >> 1;   // tiles of each stream
-        bool fin = ok && wait_bar_warp(ctl, BPV_DONE + 0, (n0 - 1) & 1, lane);
-        if (fin && n1 > 0) fin = wait_bar_warp(ctl, BPV_DONE + 1, (n1 - 1) & 1, lane);
+        (void)n0;
+        bool fin = wait_bar_warp(ctl, BPV_DONE + 0, (use0 - 1) & 1, lane);
+        if (fin && n1 > 0) fin = wait_bar_warp(ctl, BPV_DONE + 1, (use1 - 1) & 1, lane);
+        if (!fin) break;
         if (fin) {
             tc_fence_after();
             const float m = fmaxf(m_st[0], m_st[1]);
@@ -530,29 +724,23 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             const float a1 = n1 > 0 ? fast_exp2(m_st[1] - m) : 0.f;
             const float lsum = a0 * l_st[0] + a1 * l_st[1];
             const float c0 = a0 / lsum, c1 = a1 / lsum;
-            const size_t orow_idx = static_cast<size_t>(qoff + tok) * a.num_q_heads + head;
+            const size_t orow_idx = static_cast<size_t>(p.qoff + tok) * a.num_q_heads + head;
             uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * D;
-            const size_t prow = orow_idx * a.max_parts_total + r;   // cascade: slot = split
+            const size_t prow = orow_idx * a.max_parts_total + p.r;   // cascade: slot = split
             if (cascade && row_valid) {
                 a.m_part[prow] = m;   // log2 domain, as the decode partials
                 a.l_part[prow] = lsum;
             }
-            // 64 columns of both accumulators per TMEM round trip
+            // 32 columns of both accumulators per TMEM round trip
 #pragma unroll
-            for (int q2 = 0; q2 < D / 64; ++q2) {
-            float oo[2][32], o1[2][32];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-                tmem_ld32(tmem + lane_addr + kTmemO + (2 * q2 + hh) * 32, oo[hh]);
-            if (n1 > 0) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-                    tmem_ld32(tmem + lane_addr + kTmemO + 128 + (2 * q2 + hh) * 32, o1[hh]);
-            }
+            for (int q2 = 0; q2 < D / 32; ++q2) {
+            float oo[1][32], o1[1][32];
+            tmem_ld32(tmem + lane_addr + kTmemO + q2 * 32, oo[0]);
+            if (n1 > 0) tmem_ld32(tmem + lane_addr + kTmemO + 128 + q2 * 32, o1[0]);
             tmem_wait_ld();
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int q = 2 * q2 + hh;
+            for (int hh = 0; hh < 1; ++hh) {
+                const int q = q2 + hh;
                 float* o = oo[hh];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] *= c0;
@@ -580,6 +768,13 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             }
         }
+        // O of this item is read out: the issuers may start the next item's P.V.
+        tc_fence_before();
+        __syncwarp();
+        mbar_arrive_if(lane == 0, &bars[BO_FREE + 0]);
+        if (n1 > 0) mbar_arrive_if(lane == 0, &bars[BO_FREE + 1]);
+        g0 += ntiles;
+        }
     }
 
     tc_fence_before();
@@ -589,6 +784,20 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Streaming multiprocessors of the current device (read once per device).
+int sm_count() {
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (cached[dev] <= 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            return 1;
+        cached[dev] = v;
+    }
+    return cached[dev];
 }
 
 template <int D, int G>
@@ -607,8 +816,17 @@ cudaError_t launch_g(const PrefillArgs& a, cudaStream_t stream) {
         set_smem_once(reinterpret_cast<const void*>(kern), GM::kSmemBytes);
     if (e != cudaSuccess) return e;
     constexpr int TOK = kRows / G;
-    dim3 grid((a.max_new + TOK - 1) / TOK, a.num_kv_heads, a.num_reqs);
-    return launch_pdl(kern, grid, dim3(kThreads), GM::kSmemBytes, stream, mq, mk, mv, a);
+    const int qtiles = (a.max_new + TOK - 1) / TOK;
+    // Persistent CTAs walking the ranked item list, at most one per SM; not for the
+    // cascade's prefix pass, which is meant to hold few SMs beside the suffix decode.
+    const int persistent = (!a.cascade && a.num_reqs <= kMaxSchedReqs) ? 1 : 0;
+    dim3 grid(qtiles, a.num_kv_heads, a.num_reqs);
+    if (persistent) {
+        const int64_t items = static_cast<int64_t>(qtiles) * a.num_kv_heads * a.num_reqs;
+        grid = dim3(static_cast<unsigned>(items < sm_count() ? items : sm_count()), 1, 1);
+    }
+    return launch_pdl(kern, grid, dim3(kThreads), GM::kSmemBytes, stream, mq, mk, mv, a,
+                      persistent);
 }
 
 template <int D>
