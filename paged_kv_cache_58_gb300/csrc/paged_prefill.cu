@@ -203,11 +203,24 @@ PKV_DEVINL bool item_params(const PrefillArgs& a, int qt, int kvh, int r, bool r
     return true;
 }
 
+// Persistent schedule in shared memory, right after the barriers, the TMEM address and
+// the abort flag: sreq[rho] = the request of rank rho (most keys first), then off[rho] =
+// its first item (off[R] = the item count).
+constexpr int kSchedSreq = kNumBars * 8 + 16;                 // bytes past the barriers
+constexpr int kSchedOff = kSchedSreq + kMaxSchedReqs * 2;
+
 struct Sched {
-    const uint16_t* sreq;   // persistent: requests by rank (most keys first)
-    const int* off;         // persistent: off[rho] = first item of rank rho; off[R] = items
+    const uint64_t* bars;
     int R;
     bool persistent;
+    PKV_DEVINL int sreq(int rho) const {
+        return reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(bars) +
+                                                 kSchedSreq)[rho];
+    }
+    PKV_DEVINL int off(int rho) const {
+        return reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(bars) +
+                                            kSchedOff)[rho];
+    }
 };
 
 struct Cursor {
@@ -225,16 +238,16 @@ PKV_DEVINL bool next_item(const PrefillArgs& a, const Sched& s, Cursor& cur, boo
     }
     const int P = gridDim.x;
     const int b = blockIdx.x;
-    const int total = s.off[s.R];
+    const int total = s.off(s.R);
     for (;;) {
         const int m = cur.m++;
         const int k = m * P + ((m & 1) ? P - 1 - b : b);
         if (k >= total) return false;
-        while (s.off[cur.rho + 1] <= k) ++cur.rho;   // k grows with m
-        const int rem = k - s.off[cur.rho];
-        const int nq = (s.off[cur.rho + 1] - s.off[cur.rho]) / a.num_kv_heads;
+        while (s.off(cur.rho + 1) <= k) ++cur.rho;   // k grows with m
+        const int rem = k - s.off(cur.rho);
+        const int nq = (s.off(cur.rho + 1) - s.off(cur.rho)) / a.num_kv_heads;
         if (item_params<G>(a, nq - 1 - rem / a.num_kv_heads, rem % a.num_kv_heads,
-                           s.sreq[cur.rho], report, p))
+                           s.sreq(cur.rho), report, p))
             return true;
     }
 }
@@ -264,7 +277,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint16_t* sreq = reinterpret_cast<uint16_t*>(smem + GM::kOffSreq);
     int* off = reinterpret_cast<int*>(smem + GM::kOffOff);
     Ctl ctl{bars, abort_flag, a.status};
-    const Sched sch{sreq, off, a.num_reqs, persistent != 0};
+    const Sched sch{bars, a.num_reqs, persistent != 0};
 
     if (sch.persistent) {
         // Rank the requests by key count (most first, ties by index) and lay out the
@@ -574,13 +587,14 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         const float sl2 = a.scale_log2;
         Cursor cur;
         ItemParams p;
-        int g0 = 0;                  // the CTA's KV tiles before this item
-        uint32_t use0 = 0, use1 = 0;   // tiles of each stream over all items
+        uint32_t par = 0;   // bit s: parity of stream s's tiles over all items
         bool ok = true;
         while (ok && next_item<G>(a, sch, cur, false, p)) {
         const int tok = p.t0 + row / G;
-        const int head = p.kvh * G + row % G;
         const bool row_valid = tok < p.n;
+        const size_t orow_idx = static_cast<size_t>(p.qoff + tok) * a.num_q_heads +
+                                p.kvh * G + row % G;
+        const int prow_slot = p.r;
         const int lim = cascade ? p.c - 1 : (row_valid ? p.c + tok : p.c + p.n - 1);  // last key seen
         const bool p_single = p.p_single;
         const int ntiles = p.ntiles;
@@ -590,7 +604,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         float l_st[2] = {0.f, 0.f};
         for (int jt = 0; jt < ntiles; ++jt) {
             const int sm = jt & 1;
-            const uint32_t us = sm ? use1 : use0;   // this tile's use of the stream's buffers
+            const uint32_t us = (par >> sm) & 1;   // parity of this tile's use of the buffers
             const uint32_t tS = tmem + lane_addr + sm * 128;
             if (!wait_bar_warp(ctl, BS_FULL + sm, us & 1, lane)) { ok = false; break; }
             tc_fence_after();
@@ -705,7 +719,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc_fence_before();
             __syncwarp();
             mbar_arrive_if(lane == 0, &bars[BP_FULL + sm]);
-            if (sm) ++use1; else ++use0;
+            par ^= 1u << sm;
         }
         if (!ok) break;
         // ------------------------------------------------------------ epilogue
@@ -714,8 +728,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         // Stream 0 always holds key 0, which every row sees, so m_0 and l_0 are proper.
         const int n0 = (ntiles + 1) >> 1, n1 = ntiles >> 1;   // tiles of each stream
         (void)n0;
-        bool fin = wait_bar_warp(ctl, BPV_DONE + 0, (use0 - 1) & 1, lane);
-        if (fin && n1 > 0) fin = wait_bar_warp(ctl, BPV_DONE + 1, (use1 - 1) & 1, lane);
+        bool fin = wait_bar_warp(ctl, BPV_DONE + 0, (par & 1) ^ 1, lane);
+        if (fin && n1 > 0) fin = wait_bar_warp(ctl, BPV_DONE + 1, ((par >> 1) & 1) ^ 1, lane);
         if (!fin) break;
         if (fin) {
             tc_fence_after();
@@ -724,9 +738,9 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             const float a1 = n1 > 0 ? fast_exp2(m_st[1] - m) : 0.f;
             const float lsum = a0 * l_st[0] + a1 * l_st[1];
             const float c0 = a0 / lsum, c1 = a1 / lsum;
-            const size_t orow_idx = static_cast<size_t>(p.qoff + tok) * a.num_q_heads + head;
+
             uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * D;
-            const size_t prow = orow_idx * a.max_parts_total + p.r;   // cascade: slot = split
+            const size_t prow = orow_idx * a.max_parts_total + prow_slot;   // cascade: slot = split
             if (cascade && row_valid) {
                 a.m_part[prow] = m;   // log2 domain, as the decode partials
                 a.l_part[prow] = lsum;
@@ -773,7 +787,6 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         __syncwarp();
         mbar_arrive_if(lane == 0, &bars[BO_FREE + 0]);
         if (n1 > 0) mbar_arrive_if(lane == 0, &bars[BO_FREE + 1]);
-        g0 += ntiles;
         }
     }
 
