@@ -589,7 +589,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         ItemParams p;
         uint32_t par = 0;   // bit s: parity of stream s's tiles over all items
         bool ok = true;
-        while (ok && next_item<G>(a, sch, cur, false, p)) {
+        bool have = next_item<G>(a, sch, cur, false, p);
+        while (ok && have) {
         const int tok = p.t0 + row / G;
         const bool row_valid = tok < p.n;
         const size_t orow_idx = static_cast<size_t>(p.qoff + tok) * a.num_q_heads +
@@ -722,6 +723,10 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             par ^= 1u << sm;
         }
         if (!ok) break;
+        // The next item's parameters, looked up now so that their loads overlap the
+        // epilogue's waits rather than delay the next item's first tile.
+        ItemParams pn;
+        const bool have_next = next_item<G>(a, sch, cur, false, pn);
         // ------------------------------------------------------------ epilogue
         // Merge the streams: with a_s = 2^(m_s - m), m = max(m_0, m_1),
         //   O = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1).
@@ -787,6 +792,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         __syncwarp();
         mbar_arrive_if(lane == 0, &bars[BO_FREE + 0]);
         if (n1 > 0) mbar_arrive_if(lane == 0, &bars[BO_FREE + 1]);
+        p = pn;
+        have = have_next;
         }
     }
 

@@ -127,3 +127,16 @@ def test_prefill_out_of_range_block_id_raises_status(pkv, dtype):
     torch.cuda.synchronize()
     assert pkv.read_device_status() == 5
     assert pkv.read_device_status() == 0
+
+
+@pytest.mark.parametrize("num_reqs", [128, 130])
+def test_prefill_many_requests_both_schedules(pkv, oracle_mod, num_reqs):
+    """128 requests run on persistent CTAs over the request-ranked item list, 130 on one
+    CTA per query tile; ragged cached and new lengths, some requests without new tokens."""
+    rng = np.random.default_rng(num_reqs)
+    cached = [int(x) for x in rng.integers(0, 300, num_reqs)]
+    new = [int(x) for x in rng.integers(0, 40, num_reqs)]
+    new[0] = 40   # the recipe's n is max(new)
+    case = custom_case(32, 8, cached, new, seed=num_reqs, num_blocks=4096)
+    ref, _, _ = oracle_prefill_case(oracle_mod, case)
+    check_attention(run_prefill(pkv, case), ref)
