@@ -7,9 +7,9 @@
 // "Prefill Bypass").  K/V are gathered through the block table ("the kernel walks
 // the block table", Triptych "Paged Attention for Efficient Memory Management").
 //
-// One CTA computes one 128-row query tile: TOK = 128 / G consecutive new tokens x
-// the G query heads that share kv head `kvh` (rows token-major, heads inner), so
-// every K/V tile it stages serves all G heads.  Per 128-key KV tile j:
+// A work item is one 128-row query tile: TOK = 128 / G consecutive new tokens x the G
+// query heads that share kv head `kvh` (rows token-major, heads inner), so every K/V
+// tile staged for it serves all G heads.  Per 128-key KV tile j:
 //   S_j = Q K_j^T  tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) into the TMEM
 //                  S/P buffer of stream j % 2
 //   softmax        4 warps, one thread per row: tcgen05.ld S_j, causal mask, exp2,
@@ -66,8 +66,8 @@
 // are short and why one serial S/P ring left the pipe idle half the time.
 //
 // Warp roles (224 threads): warps 0-3 softmax + epilogue (warp w owns TMEM lanes
-// 32w..32w+31), warp 4 TMA producer, warp 5 TMEM owner + stream-0 issuer, warp 6
-// stream-1 issuer.  TMEM columns: S/P buffers of streams 0 and 1 at [0, 128) and
+// 32w..32w+31), warp 4 barrier set-up + TMA producer, warp 5 TMEM owner + stream-0
+// issuer, warp 6 stream-1 issuer.  TMEM columns: S/P buffers of streams 0 and 1 at [0, 128) and
 // [128, 256); their O at [256, 384) and [384, 512).
 #include <cuda.h>
 #include <cuda_runtime.h>
