@@ -260,8 +260,11 @@ pkv_status pkv_paged_decode_cascade_append(const pkv_pool_desc* pool, void* out,
  * cached_lens[r] tokens already in the pool followed by new_lens[r] new tokens whose
  * K/V must already be in the pool (kv_append first).  Query row q_offsets[r] + i
  * (i < new_lens[r]) attends keys 0 .. cached_lens[r] + i.  bf16 pools run on the
- * tcgen05 tensor cores with TMEM accumulators (bf16 in, fp32 accumulate, bf16 out); fp32
- * pools run each new token on the CUDA-core decode kernel (fp32 throughout).
+ * tcgen05 tensor cores with TMEM accumulators (bf16 in, fp32 accumulate, bf16 out), with
+ * one persistent CTA per SM when num_reqs <= 128 (one CTA per 128-row query tile
+ * otherwise); fp32 pools run on a tiled CUDA-core kernel (fp32 throughout).  A block id
+ * outside [0, num_blocks) inside a request's keys is not read and raises PKV_ERR_OOB in
+ * the device status word (that request's output is then not valid).
  *   out, q        device [total_new][num_q_heads][head_dim], the pools' dtype.
  *   block_tables  device int32 [num_reqs][max_blocks_per_seq].
  *   cached_lens, new_lens  device int32 [num_reqs]; cached >= 0, new >= 0,
