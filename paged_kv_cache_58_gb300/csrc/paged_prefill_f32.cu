@@ -88,8 +88,11 @@ PKV_DEVINL void stage_kv(float* dst, const float* pool, const int32_t* bt, int k
     }
 }
 
+// Two CTAs per SM at head_dim 128 (113 KB of shared memory each); three at head_dim 64
+// (66 KB), where the extra warps hide more shared-memory latency than the registers
+// given up for them cost (a few values spill at 80 registers).
 template <int D, int G>
-__global__ void __launch_bounds__(kFThreads, 2)
+__global__ void __launch_bounds__(kFThreads, D == 64 ? 3 : 2)
 prefill_f32_kernel(const PrefillArgs a) {
     using FG = FGeom<D>;
     constexpr int TOK = kFRows / G;
