@@ -69,6 +69,8 @@
 // 32w..32w+31), warp 4 barrier set-up + TMA producer, warp 5 TMEM owner + stream-0
 // issuer, warp 6 stream-1 issuer.  TMEM columns: S/P buffers of streams 0 and 1 at [0, 128) and
 // [128, 256); their O at [256, 384) and [384, 512).
+#include <cstdlib>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a,
-                       const int persistent) {
+                       const int persistent, const int test_stall) {
     using GM = Geom<D>;
     constexpr int TOK = kRows / G;
     extern __shared__ uint8_t smem_raw[];
@@ -382,8 +384,13 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 a.block_tables + static_cast<size_t>(cascade ? 0 : p.r) * a.max_blocks_per_seq;
             const int nchunks = p.max_lim / kChunk + 1;
             if (it >= 1 && !wait_bar_warp(ctl, BQ_EMPTY, (it - 1) & 1, lane)) break;
+            // Test hook (zero in normal use): CTA 0 arms its first Q barrier for 16 bytes
+            // more than the Q copy delivers, so the issuers' wait for it runs out of time
+            // (PKV_ERR_TIMEOUT) while the copy still lands.
+            const bool stall = test_stall && it == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
+                               blockIdx.z == 0;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bars[BQ], GM::kQBytes);
+                mbar_arrive_expect_tx(&bars[BQ], GM::kQBytes + (stall ? 16u : 0u));
 #pragma unroll
                 for (int h = 0; h < GM::kHalves; ++h)
                     tma_load_3d(smem + GM::kOffQ + h * kHalf, &tm_q, 64 * h, p.kvh * G, p.qrow0,
@@ -806,6 +813,13 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
 }
 
+// Test hook: PKV_TEST_PREFILL_STALL=1 makes one Q wait of the next prefill run out of
+// time (read at each call; tests only).
+int prefill_test_stall() {
+    const char* v = std::getenv("PKV_TEST_PREFILL_STALL");
+    return v && v[0] == '1' ? 1 : 0;
+}
+
 // Streaming multiprocessors of the current device (read once per device).
 int sm_count() {
     static int cached[64];
@@ -846,7 +860,7 @@ cudaError_t launch_g(const PrefillArgs& a, cudaStream_t stream) {
         grid = dim3(static_cast<unsigned>(items < sm_count() ? items : sm_count()), 1, 1);
     }
     return launch_pdl(kern, grid, dim3(kThreads), GM::kSmemBytes, stream, mq, mk, mv, a,
-                      persistent);
+                      persistent, prefill_test_stall());
 }
 
 template <int D>

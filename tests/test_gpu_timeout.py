@@ -52,3 +52,28 @@ def test_decode_wait_timeout_reports_status(pkv, oracle_mod, monkeypatch):
     assert pkv.read_device_status() == 0
     ref, _, _ = oracle_decode_case(oracle_mod, case)
     check_attention(out, ref)
+
+
+def test_prefill_wait_timeout_reports_status(pkv, oracle_mod, monkeypatch):
+    """The same for the tcgen05 prefill: PKV_TEST_PREFILL_STALL=1 arms CTA 0's first Q
+    barrier for 16 bytes more than the Q copy delivers.  The copy lands, the issuers'
+    wait for the barrier expires and raises the status, the CTA's other roles see the
+    abort and drain (bounded), and the next call, with the hook off, is correct."""
+    from tests.helpers import oracle_prefill_case
+    from tests.test_gpu_prefill import custom_case, run_prefill
+
+    case = custom_case(32, 8, [100, 40], [37, 64], seed=5, num_blocks=64)
+    pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+
+    monkeypatch.setenv("PKV_TEST_PREFILL_STALL", "1")
+    pkv.paged_prefill(case.q, case.k_pool, case.v_pool, case.block_tables, case.cached_lens,
+                      case.new_lens, case.q_offsets, case.scale,
+                      max_new=int(case.new_lens.max()))
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == PKV_ERR_TIMEOUT
+
+    monkeypatch.delenv("PKV_TEST_PREFILL_STALL")
+    ref, _, _ = oracle_prefill_case(oracle_mod, case)
+    check_attention(run_prefill(pkv, case), ref)   # asserts a clean status
