@@ -505,13 +505,21 @@ def main():
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # K steps back to back for the step time (an event between two steps would hold the
+    # next step's launch behind the previous one), then K more with events around each
+    # decode call for the kernel's own duration (the roofline).
     start.record(stream)
+    for _ in range(K):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
     for i in range(K):
         append(case.slot_mapping, case.k_new, case.v_new)
         ev[i][0].record(stream)
         decode(case.q, case.block_tables, case.context_lens, case.k_new, case.v_new)
         ev[i][1].record(stream)
-    end.record(stream)
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
