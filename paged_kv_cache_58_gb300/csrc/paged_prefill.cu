@@ -69,6 +69,7 @@
 // 32w..32w+31), warp 4 barrier set-up + TMA producer, warp 5 TMEM owner + stream-0
 // issuer, warp 6 stream-1 issuer.  TMEM columns: S/P buffers of streams 0 and 1 at [0, 128) and
 // [128, 256); their O at [256, 384) and [384, 512).
+#include <atomic>
 #include <cstdlib>
 
 #include <cuda.h>
@@ -822,16 +823,16 @@ int prefill_test_stall() {
 
 // Streaming multiprocessors of the current device (read once per device).
 int sm_count() {
-    static int cached[64];
+    static std::atomic<int> cached[64];   // 0: not read yet; host threads may race benignly
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-    if (cached[dev] <= 0) {
-        int v = 0;
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
             return 1;
-        cached[dev] = v;
+        cached[dev].store(v, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return v;
 }
 
 template <int D, int G>
