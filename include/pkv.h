@@ -28,7 +28,11 @@
  *    pkv_read_device_status.  The kernel calls may therefore be recorded with stream
  *    capture into a CUDA graph and replayed (make one call outside capture first, so
  *    that the per-device status word and side stream exist); pkv_paged_decode_cascade
- *    forks onto a library-owned stream and joins back within the call.
+ *    forks onto a library-owned stream and joins back within the call.  Kernels are
+ *    launched with programmatic dependent launch: a kernel may be placed on the SMs
+ *    while the stream's previous kernel finishes, but it reads no input before that
+ *    kernel has completed and its writes are visible, so inputs written by the
+ *    caller's own kernels on the same stream are safe.
  *  - Argument errors are detected on the host and returned synchronously before any
  *    launch.  A failed launch returns PKV_ERR_CUDA.  Conditions only the device can
  *    see (a slot or block id outside the pool, a pipeline wait that ran out of time)
