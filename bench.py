@@ -7,23 +7,27 @@ default both run as one call, pkv_paged_decode_append (the decode kernel stores
 and attends the new tokens); --separate-append times kv_append followed by
 paged_decode instead.
 Inputs are seeded synthetic tensors already resident in HBM.  Prints ONE JSON
-line (rank 0).
+line (rank 0).  Beside the step, the line carries measurements of the other
+published workloads on the same GPU, each with its roofline and the fp64 oracle
+timed on the host cores: the prefix-cached prefill (its kv_append alone, the
+prefill alone, and the two as one step), the Llama-3.1-70B-shaped long-context
+decode, and the shared-prefix batch through the cascade decode.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the fp64 CPU oracle (the only baseline that exists for
 this path) on the host cores, on a bounded sample of the same workload.
-Multi-GPU runs are independent replicas (the decode batch does not exchange
-data), reported as weak scaling.
+--gpus N runs N independent replicas, one process per GPU (re-launched through
+torch.distributed.run unless already under it); the decode batch exchanges no
+data, so the only cross-rank traffic is the barriers around the timed region
+and the max of its time over ranks (weak scaling).
 """
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -66,6 +70,12 @@ def parse():
     p.add_argument("--no-prefix-cache", action="store_true",
                    help="skip the host prefix-reuse measurement")
     p.add_argument("--prefill-steps", type=int, default=20)
+    p.add_argument("--no-long-decode", action="store_true",
+                   help="skip the Llama-3.1-70B-shaped long-context decode sub-line")
+    p.add_argument("--no-cascade-line", action="store_true",
+                   help="skip the shared-prefix cascade decode sub-line")
+    p.add_argument("--sub-steps", type=int, default=20,
+                   help="timed calls of each decode sub-line")
     p.add_argument("--min-warm-seconds", type=float, default=1.0,
                    help="warm-up also runs at least this long (clock sampling under load)")
     return p.parse_args()
@@ -76,6 +86,102 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_replicas(n: int, argv, script: str | None = None, stdout=None):
+    """Runs `script` (this file by default) as n processes on this node through
+    torch.distributed.run, one per GPU, rendezvous on 127.0.0.1; returns the
+    CompletedProcess.  Rank 0 prints the JSON line (passed through, or captured when
+    stdout is subprocess.PIPE)."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr=127.0.0.1", f"--master-port={_free_port()}",
+           script or os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd, stdout=stdout, text=True)
+
+
+class Ranks:
+    """The replica processes of one run (RANK, LOCAL_RANK, WORLD_SIZE and MASTER_* from
+    the environment, as torch.distributed.run sets them).  Replicas are independent: the
+    only collectives are the barriers around a timed region and the max of its time."""
+
+    def __init__(self, backend: str, device=None):
+        import torch.distributed as dist
+        self.dist = dist
+        self.ws, self.rank, self.local = dist_env()
+        self.device = device
+        if self.ws > 1:
+            dist.init_process_group(backend)
+
+    def barrier(self):
+        if self.ws > 1:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.ws == 1:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.ws > 1:
+            self.dist.destroy_process_group()
+
+
+class EventClock:
+    """Seconds between two CUDA events on the launching stream (synchronised)."""
+
+    def __init__(self, stream):
+        import torch
+        self.torch, self.stream = torch, stream
+
+    def sync(self):
+        self.torch.cuda.synchronize()
+
+    def begin(self):
+        self.a = self.torch.cuda.Event(enable_timing=True)
+        self.b = self.torch.cuda.Event(enable_timing=True)
+        self.a.record(self.stream)
+
+    def end(self) -> float:
+        self.b.record(self.stream)
+        self.torch.cuda.synchronize()
+        return self.a.elapsed_time(self.b) * 1e-3
+
+
+class WallClock:
+    """Host seconds around work that synchronises itself (the end-to-end steps)."""
+
+    def sync(self):
+        pass
+
+    def begin(self):
+        self.t0 = time.perf_counter()
+
+    def end(self) -> float:
+        return time.perf_counter() - self.t0
+
+
+def replica_rate(ranks: Ranks, step, K: int, units_per_step: float, clock):
+    """K steps back to back, with a barrier and a synchronisation on both sides; returns
+    (whole-job units per second, max over ranks of the elapsed seconds): the work of all
+    ranks over the slowest rank's time."""
+    ranks.barrier()
+    clock.sync()
+    clock.begin()
+    for _ in range(K):
+        step()
+    el = clock.end()
+    ranks.barrier()
+    return aggregate(el, units_per_step * K, ranks.ws, ranks.max)
 
 
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -102,14 +208,55 @@ def prefill_flops(case):
     return 4 * D * Hq * total
 
 
-def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf16"):
+class L2Flush:
+    """Writes a buffer of twice the L2 size, evicting what earlier calls left in L2, for
+    timed calls whose bytes would otherwise fit in it."""
+
+    def __init__(self, dev):
+        import torch
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size or (129 << 20)
+        self.buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def time_calls(call, steps, stream, before=None):
+    """Mean seconds of `call` over `steps` launches, CUDA events around each on the
+    launching stream; `before` (an L2 flush) runs ahead of each start event."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        if before is not None:
+            before()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e-3
+
+
+def append_bytes_of(k_new, slot_mapping):
+    """Algorithmic bytes of one kv_append: the new K and V rows read, the same bytes
+    written into the pools, and the slot mapping read."""
+    return 2 * 2 * k_new.numel() * k_new.element_size() + \
+        slot_mapping.numel() * slot_mapping.element_size()
+
+
+def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf16",
+                  peaks_=None, cpu=True):
     """Prefix-cached chunked prefill (16 requests x 512 new tokens over cached
-    prefixes of U[1024, 8192]): kv_append of the new rows, then timed prefill calls
-    (CUDA events on the launching stream, K/V of 335 MB per call > L2).  block_size,
-    head_dim and dtype vary the recipe (the pool keeps its byte size)."""
+    prefixes of U[1024, 8192]) measured three ways: the kv_append of the 8192 new rows
+    alone (L2 flushed before each call: its 67 MB fit in L2), the prefill call alone
+    (K/V of 335 MB per call > L2), and the workload's step, append then prefill, K
+    times back to back.  block_size, head_dim and dtype vary the recipe (the pool keeps
+    its byte size).  With `cpu` the oracle prefill is timed on the host cores over the
+    first requests of the batch."""
     import dataclasses
     import torch
     import synth
+    hbm, tpeak, kind = peaks_ or peaks()
     wl = synth.WORKLOADS["prefill"]
     over = {}
     if block_size and block_size != wl.block_size:
@@ -124,36 +271,204 @@ def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf
             f"_{k}{v}" for k, v in (("B", over.get("block_size")), ("D", over.get("head_dim")),
                                     ("", "f32" if dtype == "fp32" else None)) if v), **over)
     case = synth.build_case(wl, dev)
-    pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new,
-                  stream=stream)
     out = torch.empty_like(case.q)
     max_new = int(case.new_lens.max())
+
+    def append():
+        pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new,
+                      stream=stream)
 
     def call():
         pkv.paged_prefill(case.q, case.k_pool, case.v_pool, case.block_tables,
                           case.cached_lens, case.new_lens, case.q_offsets, case.scale,
                           max_new=max_new, out=out, stream=stream)
 
+    def step():
+        append()
+        call()
+
     for _ in range(3):
-        call()
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    for a, b in evs:
-        a.record(stream)
-        call()
-        b.record(stream)
+        step()
     torch.cuda.synchronize()
     assert pkv.read_device_status() == 0
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    ms = time_calls(call, steps, stream) * 1e3
+    flush = L2Flush(dev)
+    append_s = time_calls(append, steps, stream, before=flush)
+    clock = EventClock(stream)
+    clock.sync()
+    clock.begin()
+    for _ in range(steps):
+        step()
+    step_s = clock.end() / steps
+    assert pkv.read_device_status() == 0
+    del flush
     flops = prefill_flops(case)
+    esz = case.q.element_size()
     kv_bytes = int((case.context_lens.to(torch.int64)).sum()) * case.k_pool.shape[1] * \
-        case.q.shape[2] * case.q.element_size() * 2
+        case.q.shape[2] * esz * 2
+    ab = append_bytes_of(case.k_new, case.slot_mapping)
     res = {"workload": case.wl.name, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
            "flops_per_call": flops, "kv_bytes_per_call": kv_bytes, "launches": steps,
            "block_size": case.k_pool.shape[2], "head_dim": case.q.shape[2],
-           "dtype": "f32" if case.q.element_size() == 4 else "bf16"}
+           "dtype": "f32" if esz == 4 else "bf16",
+           "step": {"calls": "kv_append (8192 new rows) + paged_prefill, back to back",
+                    "ms": step_s * 1e3, "tflops": flops / step_s / 1e12, "steps": steps,
+                    "gpu_launches": 2 * steps},
+           "append": {"kernel": "kv_append_kernel", "rows": int(case.k_new.shape[0]),
+                      "bytes_per_call": ab, "ms": append_s * 1e3,
+                      "l2": "flushed before each call (2 x L2 written)",
+                      "roofline": {"bound": "hbm", "achieved": ab / append_s / 1e9,
+                                   "peak": hbm, "unit": "GB/s",
+                                   "frac": ab / append_s / 1e9 / hbm,
+                                   "peak_kind": f"{kind} hbm_gbs",
+                                   "frac_of_8tbs": ab / append_s / 1e9 / NOMINAL_HBM_GBS,
+                                   "traffic": None}}}
+    if cpu:
+        res["cpu_baseline"] = prefill_cpu_baseline(case, flops)
     del case, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def prefill_cpu_baseline(case, flops_all, budget_s=10.0):
+    """The oracle prefill on the host cores over the batch's first requests (the number
+    sized so that the repeated passes take about `budget_s`), in TFLOP/s of the same
+    algorithmic flops the GPU figure counts."""
+    import numpy as np
+    import oracle
+    import synth
+    oracle.build()
+    kp, vp = synth.host_bits(case.k_pool), synth.host_bits(case.v_pool)
+    q, bt = synth.host_bits(case.q), synth.host_bits(case.block_tables)
+    cl, nl = synth.host_bits(case.cached_lens), synth.host_bits(case.new_lens)
+    qo = synth.host_bits(case.q_offsets)
+    D, Hq = q.shape[2], q.shape[1]
+
+    def run(nr):
+        rows = int(qo[nr])
+        t0 = time.perf_counter()
+        oracle.paged_prefill(q[:rows], kp, vp, bt[:nr], cl[:nr], nl[:nr], qo[:nr + 1],
+                             case.scale)
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    nr = int(max(1, min(len(cl), budget_s / 2 / max(t1, 1e-9))))
+    reps, el = 0, 0.0
+    while el < budget_s / 2 or reps < 1:
+        el += run(nr)
+        reps += 1
+    sub = 4 * D * Hq * sum(int(n) * int(c) + int(n) * (int(n) + 1) // 2
+                           for c, n in zip(cl[:nr], nl[:nr]))
+    return {"value": sub * reps / el / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"first {nr} of {len(cl)} requests ({sub / 1e9:.1f} of "
+                      f"{flops_all / 1e9:.0f} GFLOP), {reps} passes in {el:.1f} s; fp64, "
+                      "std::thread over (request, kv head)"}
+
+
+def decode_cpu_baseline(case, bytes_all, tokens_all, budget_s=8.0):
+    """The oracle decode on the host cores over the batch's first sequences (sized so the
+    repeated passes take about `budget_s`), in GB/s of the same algorithmic bytes the GPU
+    figure counts, scaled by the sample's share of the attended tokens."""
+    import numpy as np
+    import oracle
+    import synth
+    oracle.build()
+    kp, vp = synth.host_bits(case.k_pool), synth.host_bits(case.v_pool)
+    oracle.kv_append(synth.host_bits(case.slot_mapping), synth.host_bits(case.k_new),
+                     synth.host_bits(case.v_new), kp, vp)
+    q, bt = synth.host_bits(case.q), synth.host_bits(case.block_tables)
+    cl = synth.host_bits(case.context_lens)
+
+    def run(n):
+        t0 = time.perf_counter()
+        oracle.paged_decode(q[:n], kp, vp, bt[:n], cl[:n], case.scale)
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    n = int(max(1, min(len(cl), budget_s / 2 / max(t1, 1e-9))))
+    reps, el = 0, 0.0
+    while el < budget_s / 2 or reps < 1:
+        el += run(n)
+        reps += 1
+    tok = int(cl[:n].astype(np.int64).sum())
+    sub_bytes = bytes_all * tok / max(tokens_all, 1)
+    return {"value": sub_bytes * reps / el / 1e9, "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle", "tokens_per_s_per_layer": n * reps / el,
+            "sample": f"first {n} of {len(cl)} sequences ({tok} of {tokens_all} tokens, all "
+                      f"heads), {reps} passes in {el:.1f} s; fp64, std::thread over "
+                      "(sequence, kv head)"}
+
+
+def bench_decode_line(pkv, dev, name, steps, stream, peaks_, cascade=False, cpu=True):
+    """One published decode workload through its fused call (append + decode, or the
+    cascade decode with the append for the shared-prefix batch), timed per call with
+    CUDA events; its GB/s on the unique bytes against the HBM roofline, the logical rate,
+    tokens/s, and the oracle on the host cores."""
+    import torch
+    import synth
+    hbm, _, kind = peaks_
+    case = synth.build_case(name, dev)
+    S, Hq, D = case.q.shape
+    B = case.k_pool.shape[2]
+    decode_bytes, append_bytes, tokens, unique = workload_bytes(case)
+    append_bytes -= case.slot_mapping.numel() * case.slot_mapping.element_size()  # fused
+    max_ctx = case.max_context
+    out = torch.empty_like(case.q)
+    if cascade:
+        plen = case.wl.shared_prefix
+        prefix_blocks = case.block_tables[0, :plen // B].contiguous()
+        ws = torch.empty(max(16, pkv.cascade_workspace_bytes(S, Hq, D, plen, max_ctx,
+                                                             block_size=B)),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            pkv.paged_decode_cascade_append(case.q, case.k_pool, case.v_pool, case.k_new,
+                                            case.v_new, prefix_blocks, plen,
+                                            case.block_tables, case.context_lens, case.scale,
+                                            max_context=max_ctx, out=out, workspace=ws,
+                                            stream=stream)
+        kernel = ("paged_decode_cascade_append (tcgen05 prefix pass on a side stream + suffix "
+                  "split-KV decode with the append + combine)")
+        launches = 3
+    else:
+        pb = pkv.auto_partition(S, Hq, max_ctx, block_size=B)
+        ws = torch.empty(max(16, pkv.decode_workspace_bytes(S, Hq, D, max_ctx, pb,
+                                                            block_size=B)),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            pkv.paged_decode_append(case.q, case.k_pool, case.v_pool, case.k_new, case.v_new,
+                                    case.block_tables, case.context_lens, case.scale,
+                                    max_context=max_ctx, out=out, partition_blocks=pb,
+                                    workspace=ws, stream=stream)
+        kernel = "paged_decode_append (decode_tc split-KV with the append + combine)"
+        launches = 2
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    sec = time_calls(call, steps, stream)
+    assert pkv.read_device_status() == 0
+    call_bytes = unique + append_bytes
+    achieved = call_bytes / sec / 1e9
+    res = {"workload": case.wl.name, "num_seqs": S, "q_heads": Hq,
+           "kv_heads": case.k_pool.shape[1], "head_dim": D, "block_size": B,
+           "mean_context": tokens / S, "max_context": max_ctx, "ms": sec * 1e3,
+           "calls": steps, "gpu_launches": launches * steps,
+           "tokens_per_s_per_layer": S / sec,
+           "logical_gbs": (decode_bytes + append_bytes) / sec / 1e9,
+           "kv_bytes_per_call": decode_bytes, "unique_kv_bytes_per_call": unique,
+           "l2": ("K/V per call larger than L2" if unique > 2 * 129e6
+                  else "K/V per call fits in L2: warm-cache figure"),
+           "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm,
+                        "unit": "GB/s", "frac": achieved / hbm,
+                        "peak_kind": f"{kind} hbm_gbs", "bytes_per_launch": call_bytes,
+                        "frac_of_8tbs": achieved / NOMINAL_HBM_GBS, "traffic": None}}
+    if cpu:
+        res["cpu_baseline"] = decode_cpu_baseline(case, decode_bytes + append_bytes, tokens)
+    del case, out, ws
+    torch.cuda.empty_cache()
     return res
 
 
@@ -252,33 +567,11 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-# Files the tensor-core decode kernel is compiled from (its ncu record names their sha1).
-DECODE_TC_SOURCES = ("paged_decode_tc.cu", "common.cuh", "kernels.h")
-
-
-def kernel_traffic(kernel_srcs, summary: str):
-    """DRAM bytes per launch recorded by an ncu capture of exactly these kernel sources
-    (sha1 over the files in order); None once any of them changed."""
-    try:
-        h = hashlib.sha1()
-        for f in kernel_srcs:
-            h.update(open(f, "rb").read())
-        digest = h.hexdigest()[:12]
-        text = open(summary).read()
-    except OSError:
-        return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)\s*\(source sha1 ([0-9a-f]+)",
-                  text)
-    if m and m.group(2) == digest:
-        return float(m.group(1))
-    return None
-
-
 def aggregate(elapsed: float, units_per_rank: float, ws: int, all_reduce_max=None):
     """Whole-job rate over `ws` independent replicas: the time is the slowest rank's
     (max over ranks), the work the sum over ranks.  `all_reduce_max` maps a local float
     to the max over ranks (None: one rank)."""
-    t = all_reduce_max(elapsed) if all_reduce_max else elapsed
+    t = all_reduce_max(elapsed) if all_reduce_max and ws > 1 else elapsed
     return ws * units_per_rank / t, t
 
 
@@ -411,21 +704,21 @@ def main():
     if args.impl == "reference":
         run_reference(args, ws, rank)
         return
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # N replicas, one process per GPU, through torch.distributed.run
+        sys.exit(launch_replicas(args.gpus, sys.argv[1:]).returncode)
 
     import torch
-    import torch.distributed as dist
-    if ws > 1:
-        dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    ranks = Ranks("nccl", dev)
 
     import synth
     import paged_kv_cache_58_gb300 as pkv
     from paged_kv_cache_58_gb300 import build as pkv_build
     if rank == 0 or ws == 1:
         pkv_build.build()
-    if ws > 1:
-        dist.barrier()
+    ranks.barrier()
 
     wl = synth.WORKLOADS[args.workload]
     if args.block_size and args.block_size != wl.block_size:
@@ -498,45 +791,23 @@ def main():
     assert pkv.read_device_status() == 0
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    step_bytes = decode_bytes + append_bytes
     # K steps back to back for the step time (an event between two steps would hold the
     # next step's launch behind the previous one), then K more with events around each
     # decode call for the kernel's own duration (the roofline).
-    start.record(stream)
-    for _ in range(K):
-        step()
-    end.record(stream)
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
+    rate, total_s = replica_rate(ranks, step, K, step_bytes, EventClock(stream))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
     for i in range(K):
         append(case.slot_mapping, case.k_new, case.v_new)
         ev[i][0].record(stream)
         decode(case.q, case.block_tables, case.context_lens, case.k_new, case.v_new)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
+    ranks.barrier()
     clk = clocks.stop()
-    total_ms = start.elapsed_time(end)
     decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-
-    def max_over_ranks(x: float) -> float:
-        t = torch.tensor([x], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    reducer = max_over_ranks if ws > 1 else None
     assert pkv.read_device_status() == 0
-
-    step_bytes = decode_bytes + append_bytes
-    rate, total_s = aggregate(total_ms * 1e-3, step_bytes * K, ws, reducer)
     value = rate / 1e9
     ms_step = total_s * 1e3 / K
     tok_s = ws * S * K / total_s
@@ -602,37 +873,28 @@ def main():
 
         for _ in range(max(3, args.warmup)):
             e2e_step()
-        if ws > 1:
-            dist.barrier()
-        t0 = time.perf_counter()
-        for _ in range(K):
-            e2e_step()
-        el = time.perf_counter() - t0
-        e2e_rate, el = aggregate(el, step_bytes * K, ws, reducer)
+        e2e_rate, el = replica_rate(ranks, e2e_step, K, step_bytes, WallClock())
         e2e = {"value": e2e_rate / 1e9, "unit": "GB/s", "api": e2e_api,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": el / K * 1e3, "tokens_per_s_per_layer": ws * S * K / el}
 
     if rank != 0:
-        if ws > 1:
-            dist.destroy_process_group()
+        ranks.close()
         return
 
-    peak, tpeak, peak_kind = peaks()
+    pk = peaks()
+    peak, tpeak, peak_kind = pk
     # Roofline on the unique bytes: a shared prefix is read from HBM once per step and
     # from L2 by every other sequence, so the logical rate can exceed HBM bandwidth.  The
     # fused call also moves the new rows (read from the input, stored into the pool).
     call_bytes = unique_bytes + (append_bytes if fused else 0)
     achieved = call_bytes / (decode_ms * 1e-3) / 1e9
-    traffic = None
-    if args.workload == "8b" and case.q.dtype.itemsize == 2:
-        csrc = os.path.join(ROOT, "paged_kv_cache_58_gb300", "csrc")
-        traffic = kernel_traffic([os.path.join(csrc, f) for f in DECODE_TC_SOURCES],
-                                 os.path.join(ROOT, "profiles", "paged_decode_tc_llama3_8b.md"))
+    del workspace, out
     prefill = None
     if not args.no_prefill:
         prefill = bench_prefill(pkv, dev, args.prefill_steps, stream, args.block_size,
-                                args.prefill_head_dim, args.prefill_dtype)
+                                args.prefill_head_dim, args.prefill_dtype, pk,
+                                cpu=not args.no_cpu_baseline)
         if prefill["dtype"] == "f32":
             # fp32 pools run on the CUDA cores: fp32 FMA peak from the unit counts and the
             # maximum SM clock (152 SMs x 128 FMA a clock x 2 flop x 2.07 GHz).
@@ -644,10 +906,18 @@ def main():
             prefill.update({"bound": "tensor", "peak": tpeak, "unit": "TFLOP/s",
                             "frac": prefill["tflops"] / tpeak,
                             "peak_kind": f"{peak_kind} bf16_tflops (burst; kernel timed alone)"})
+    long_decode = cascade_line = None
+    if not args.no_long_decode and args.workload != "70b":
+        long_decode = bench_decode_line(pkv, dev, "70b", args.sub_steps, stream, pk,
+                                        cpu=not args.no_cpu_baseline)
+    if not args.no_cascade_line and not (args.workload == "shared" and cascade):
+        cascade_line = bench_decode_line(pkv, dev, "shared", args.sub_steps, stream, pk,
+                                         cascade=True, cpu=not args.no_cpu_baseline)
+    dtype = {torch.bfloat16: "bf16", torch.float32: "f32"}[case.q.dtype]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
         "pct_of_8tbs": 100.0 * value / ws / NOMINAL_HBM_GBS,
         "tokens_per_s_per_layer": tok_s,
         "config": {"workload": case.wl.name, "num_seqs": S, "q_heads": Hq,
@@ -677,9 +947,11 @@ def main():
                                     (decode_ms * 1e-3) / 1e9,
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
-                     "decode_ms": decode_ms, "traffic": traffic},
+                     "decode_ms": decode_ms, "traffic": None},
         "e2e": e2e,
         "prefill": prefill,
+        "long_decode": long_decode,
+        "shared_prefix_cascade": cascade_line,
         "prefix_cache": None if args.no_prefix_cache else bench_prefix_cache(pkv),
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
@@ -687,8 +959,7 @@ def main():
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, decode_bytes, tokens)
     print(json.dumps(line), flush=True)
-    if ws > 1:
-        dist.destroy_process_group()
+    ranks.close()
 
 
 if __name__ == "__main__":

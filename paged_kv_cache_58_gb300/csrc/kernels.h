@@ -72,7 +72,7 @@ struct DecodeArgs {
     // CTAs take no SM before the stream's previous kernel has ended (the cascade decode:
     // the prefix pass on the side stream is placed first).
     int no_pdl;
-    // Test hook (tensor-core decode): nonzero makes warp 0 of CTA (0, 0, 0) arm its first
+    // Test hook (both decode kernels): nonzero makes warp 0 of CTA (0, 0, 0) arm its first
     // stage for 16 bytes more than the stage's copies deliver, so that wait runs out of
     // time (PKV_ERR_TIMEOUT) while every copy still lands.  Zero in normal use.
     int test_stall;
@@ -84,6 +84,20 @@ struct DecodeArgs {
     const void* k_new;
     const void* v_new;
 };
+
+#ifdef __CUDACC__
+// Zeros of the G output rows (kv head kvh's query heads) of sequence `seq`, elem_bytes
+// per element, stored 16 bytes at a time by the threads of the calling CTA; for a
+// sequence the decode kernels reject (context length below 1), so that its rows hold no
+// stale memory.
+__device__ __forceinline__ void zero_invalid_rows(const DecodeArgs& a, int seq, int kvh, int G,
+                                                  int D, int elem_bytes) {
+    const size_t row0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.out) + row0 * D * elem_bytes);
+    const int n16 = G * D * elem_bytes / 16;
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+}
+#endif
 
 // CUDA-core decode (fp32 and bf16 pools): split kernel + combine.
 cudaError_t launch_paged_decode(const DecodeArgs& a, int dtype, int head_dim, int group,

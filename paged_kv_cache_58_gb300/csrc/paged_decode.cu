@@ -190,6 +190,11 @@ decode_split_kernel(const DecodeArgs a) {
         // suffix; one inside the shared prefix is not stored: report it.
         if (append && part == 0 && threadIdx.x == 0 && L > 0 && nblk <= a.chunk_offset)
             raise_status(a.status, PKV_ERR_INVALID);
+        // A context length below 1 is outside the contract (a query sees at least its own
+        // key): report it, and give the sequence's rows zeros rather than stale memory.
+        if (L <= 0 && part == 0 && threadIdx.x == 0) raise_status(a.status, PKV_ERR_INVALID);
+        if (L <= 0 && part == 0 && a.chunk_offset == 0)
+            zero_invalid_rows(a, seq, kvh, G, D, static_cast<int>(sizeof(T)));
         return;
     }
     const int b1 = min(nblk, b0 + a.partition_chunks);
@@ -234,7 +239,10 @@ decode_split_kernel(const DecodeArgs a) {
         const int ci = my_first + i * kWarps;   // chunk: rows 16 (ci & mask) of its block
         const size_t off = (((static_cast<size_t>(phys) * a.num_kv_heads + kvh) << a.chunk_shift) +
                             (ci & ((1 << a.chunk_shift) - 1))) * kBlock * D;
-        mbar_arrive_expect_tx(bar, SM::kStageBytes);
+        // test hook: 16 bytes more than the copies deliver (see DecodeArgs::test_stall)
+        const bool stall = a.test_stall && i == 0 && warp == 0 && blockIdx.x == 0 &&
+                           blockIdx.y == 0 && blockIdx.z == 0;
+        mbar_arrive_expect_tx(bar, SM::kStageBytes + (stall ? 16u : 0u));
         bulk_g2s(st, kpool + off, SM::kSlab, bar);
         bulk_g2s(st + SM::kSlab, vpool + off, SM::kSlab, bar);
     };

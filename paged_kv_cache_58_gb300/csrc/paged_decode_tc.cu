@@ -144,6 +144,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         // suffix; one inside the shared prefix is not stored: report it.
         if (append && part == 0 && threadIdx.x == 0 && L > 0 && nblk <= a.chunk_offset)
             raise_status(a.status, PKV_ERR_INVALID);
+        // A context length below 1 is outside the contract (a query sees at least its own
+        // key): report it, and give the sequence's rows zeros rather than stale memory.
+        if (L <= 0 && part == 0 && threadIdx.x == 0) raise_status(a.status, PKV_ERR_INVALID);
+        if (L <= 0 && part == 0 && a.chunk_offset == 0)
+            zero_invalid_rows(a, seq, kvh, G, D, 2);   // bf16 output
         return;
     }
     const int b1 = min(nblk, b0 + a.partition_chunks);

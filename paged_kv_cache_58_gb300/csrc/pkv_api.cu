@@ -89,7 +89,8 @@ int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 // 81 %, 32: 89 %, 64: 90 % of the copy bandwidth) -- and at most 64 partitions per
 // sequence to bound the workspace; shrink partitions (down to 8 chunks) while fewer
 // than 2 x 152 CTAs would be busy.  The result is a multiple of 4 chunks (one per warp
-// per step) and of 2 (a whole number of 32-token blocks).
+// per step) and so of 2 (a whole number of 32-token blocks): each halving rounds up to
+// a multiple of 4.
 // The CTA estimate counts ceil(Hq / 8) kv heads per sequence (a lower bound: a
 // GQA group is at most 8 query heads) so that the choice, and with it the
 // workspace size, depends only on (num_seqs, num_q_heads, max_context).
@@ -101,7 +102,7 @@ int auto_partition_chunks(int num_seqs, int num_q_heads, int max_context) {
     pc = (pc + 3) / 4 * 4;
     while (pc > 8 && static_cast<int64_t>(num_seqs) * kv_heads_min * ceil_div(max_chunks, pc) <
                          304)
-        pc /= 2;
+        pc = (pc / 2 + 3) / 4 * 4;
     return pc;
 }
 
@@ -127,8 +128,8 @@ int prefill_p_single_min_keys() {
     return (v != nullptr && std::strcmp(v, "split") == 0) ? INT_MAX : kPSingleMinKeys;
 }
 
-// PKV_TEST_DECODE_STALL=1 arms the tensor-core decode's timeout test hook (one wait of
-// one warp runs out of time; read at each call; tests only).
+// PKV_TEST_DECODE_STALL=1 arms the decode kernels' timeout test hook (one wait of one
+// warp runs out of time; read at each call; tests only).
 int decode_test_stall() {
     const char* v = std::getenv("PKV_TEST_DECODE_STALL");
     return v != nullptr && std::strcmp(v, "1") == 0;
@@ -295,10 +296,9 @@ pkv_status decode_impl(const pkv_pool_desc* pool, void* out, const void* q, cons
         a.l_part = reinterpret_cast<float*>(w + rows * pool->head_dim * sizeof(float) + ml);
     }
     const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
-    if (pool->dtype == PKV_BF16 && !decode_use_simt()) {
-        a.test_stall = decode_test_stall();
+    a.test_stall = decode_test_stall();
+    if (pool->dtype == PKV_BF16 && !decode_use_simt())
         return from_cuda(pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_));
-    }
     return from_cuda(pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_));
 }
 
@@ -563,9 +563,31 @@ pkv_status cascade_impl(const pkv_pool_desc* pool, void* out, const void* q, con
     } ev{fork, join};
     if (cudaEventRecord(fork, st_) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
         return PKV_ERR_CUDA;
+    // From here on the side stream carries this call's work: every exit, the error
+    // returns included, makes the caller's stream wait for it, so that no work of the call
+    // runs on past its return unordered with the caller's stream, and a stream capture
+    // ends with the side stream joined back.
+    struct Rejoin {
+        cudaStream_t side, st;
+        cudaEvent_t ev;
+        bool recorded = false, waited = false;
+        cudaError_t record() {
+            recorded = true;
+            return cudaEventRecord(ev, side);
+        }
+        cudaError_t wait() {
+            cudaError_t e = recorded ? cudaSuccess : record();
+            waited = true;
+            const cudaError_t w = cudaStreamWaitEvent(st, ev, 0);
+            return e != cudaSuccess ? e : w;
+        }
+        ~Rejoin() {
+            if (!waited) wait();
+        }
+    } rejoin{side, st_, join};
     cudaError_t e = pkv::launch_paged_prefill(pa, group, side);
     if (e != cudaSuccess) return e == cudaErrorNotSupported ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
-    if (cudaEventRecord(join, side) != cudaSuccess) return PKV_ERR_CUDA;
+    if (rejoin.record() != cudaSuccess) return PKV_ERR_CUDA;
 
     // 2. private suffixes (blocks from prefix_len / B on) + 3. log-sum-exp merge
     pkv::DecodeArgs a{};
@@ -596,8 +618,8 @@ pkv_status cascade_impl(const pkv_pool_desc* pool, void* out, const void* q, con
     a.v_new = v_new;
     e = decode_use_simt() ? pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_)
                           : pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_);
-    if (e != cudaSuccess) return PKV_ERR_CUDA;
-    if (cudaStreamWaitEvent(st_, join, 0) != cudaSuccess) return PKV_ERR_CUDA;
+    if (e != cudaSuccess) return e == cudaErrorNotSupported ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
+    if (rejoin.wait() != cudaSuccess) return PKV_ERR_CUDA;
     return from_cuda(pkv::launch_decode_combine(a, pool->dtype, pool->head_dim, st_));
 }
 

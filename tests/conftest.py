@@ -17,3 +17,24 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def published_decode_ref(oracle_mod):
+    """Oracle output of a whole published decode batch ("70b", "shared"), computed once
+    per session: the batch is drawn on the GPU (its generator fixes the values), the
+    oracle runs on host copies after the step's append."""
+    import torch
+
+    import synth
+    from tests.helpers import oracle_decode_case
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            case = synth.build_case(name, "cuda")
+            cache[name], _, _ = oracle_decode_case(oracle_mod, case)
+            del case
+            torch.cuda.empty_cache()
+        return cache[name]
+    return get

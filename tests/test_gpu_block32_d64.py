@@ -11,8 +11,8 @@ import pytest
 import torch
 
 import synth
-from tests.helpers import (check_attention, oracle_decode_case, oracle_prefill_case,
-                           pool_equal, to_f64)
+from tests.helpers import (case_single_p, check_attention, oracle_decode_case,
+                           oracle_prefill_case, pool_equal, to_f64)
 from tests.test_gpu_prefill import custom_case, run_prefill
 
 pytestmark = pytest.mark.gpu
@@ -125,7 +125,7 @@ def test_prefill_d64_and_block32(pkv, oracle_mod, d, bs, hq, hkv):
     ref, kp, vp = oracle_prefill_case(oracle_mod, case)
     out = run_prefill(pkv, case)
     assert pool_equal(case.k_pool, kp) and pool_equal(case.v_pool, vp)
-    check_attention(out, ref)
+    check_attention(out, ref, single_p=case_single_p(case))
 
 
 @pytest.mark.parametrize("d,bs", [(64, 16), (64, 32), (128, 32)])
@@ -134,7 +134,7 @@ def test_prefill_edges_d64_block32(pkv, oracle_mod, d, bs):
         case = custom_case(32, 8, cached, new, seed=cached[0] + new[0] + d, head_dim=d,
                            block_size=bs)
         ref, _, _ = oracle_prefill_case(oracle_mod, case)
-        check_attention(run_prefill(pkv, case), ref)
+        check_attention(run_prefill(pkv, case), ref, single_p=case_single_p(case))
 
 
 @pytest.mark.parametrize("d,bs,hq,hkv", [(64, 16, 8, 2), (128, 16, 32, 8), (64, 32, 4, 4),

@@ -115,18 +115,15 @@ def test_fused_llama3_8b_full(pkv, oracle_mod, kernel):
     check_attention(out, ref)
 
 
-@pytest.mark.parametrize("wl_name,n_rows", [("70b", 24), ("shared", 64)])
-def test_fused_full_size_sampled(pkv, oracle_mod, wl_name, n_rows):
+@pytest.mark.parametrize("wl_name", ["70b", "shared"])
+def test_fused_full_size(pkv, published_decode_ref, wl_name):
     """The 70B long-context and shared-prefix batches at full size through the fused
-    call (as the bench times them); sampled (sequence, head) outputs vs the oracle and
-    every new slot stored."""
+    call (as the bench times them): every output against the oracle and every new slot
+    stored."""
+    ref = published_decode_ref(wl_name)
     case = synth.build_case(wl_name, "cuda")
-    S, Hq = case.q.shape[:2]
-    want = synth.sample_rows(S, Hq, n_rows, seed=5)
-    ref, _, _ = oracle_decode_case(oracle_mod, case, want=want)
     out = fused(pkv, case)
-    check_attention(out, ref, mask=want)
-    assert torch.isfinite(out.float()).all()
+    check_attention(out, ref)
     B = case.k_pool.shape[2]
     blk, off = case.slot_mapping // B, case.slot_mapping % B
     assert torch.equal(case.k_pool[blk, :, off], case.k_new)

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import synth
-from tests.helpers import check_attention, oracle_decode_case, pool_equal
+from tests.helpers import case_single_p, check_attention, oracle_decode_case, pool_equal
 
 pytestmark = pytest.mark.gpu
 
@@ -92,4 +92,4 @@ def test_random_prefill_config(pkv, oracle_mod, i):
     ref, kp, vp = oracle_prefill_case(oracle_mod, case)
     out = run_prefill(pkv, case)
     assert pool_equal(case.k_pool, kp) and pool_equal(case.v_pool, vp)
-    check_attention(out, ref)
+    check_attention(out, ref, single_p=case_single_p(case))

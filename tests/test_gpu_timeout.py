@@ -1,9 +1,9 @@
 """The bounded pipeline wait on a GPU: a wait that runs out of time reports
 PKV_ERR_TIMEOUT through the device status word and leaves the context usable.
 
-The test hook PKV_TEST_DECODE_STALL=1 makes one warp of one CTA of the tensor-core
-decode arm its first stage's barrier for 16 bytes more than that stage's copies
-deliver.  All copies land; the barrier phase never completes, so that warp's wait
+The test hook PKV_TEST_DECODE_STALL=1 makes one warp of one CTA of the decode
+kernel (tensor-core or CUDA-core) arm its first stage's barrier for 16 bytes more
+than that stage's copies deliver.  All copies land; the barrier phase never completes, so that warp's wait
 expires after its time budget (2 s), raises the status, drains its other stage and
 finishes.  Nothing faults, traps or loops without a limit."""
 import dataclasses
@@ -29,8 +29,14 @@ def pkv():
     return m
 
 
-def test_decode_wait_timeout_reports_status(pkv, oracle_mod, monkeypatch):
-    monkeypatch.delenv("PKV_DECODE_KERNEL", raising=False)
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+def test_decode_wait_timeout_reports_status(pkv, oracle_mod, monkeypatch, kernel):
+    """Both decode kernels: the tensor-core one (TMA boxes, converged-warp waits) and the
+    CUDA-core one (bulk copies, per-lane waits)."""
+    if kernel == "simt":
+        monkeypatch.setenv("PKV_DECODE_KERNEL", "simt")
+    else:
+        monkeypatch.delenv("PKV_DECODE_KERNEL", raising=False)
     wl = dataclasses.replace(synth.WORKLOADS["8b"], num_blocks=256)
     case = synth.build_case(wl, "cuda", lengths=[100, 37, 300], seed=3)
     pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new)
@@ -76,4 +82,4 @@ def test_prefill_wait_timeout_reports_status(pkv, oracle_mod, monkeypatch):
 
     monkeypatch.delenv("PKV_TEST_PREFILL_STALL")
     ref, _, _ = oracle_prefill_case(oracle_mod, case)
-    check_attention(run_prefill(pkv, case), ref)   # asserts a clean status
+    check_attention(run_prefill(pkv, case), ref)   # asserts a clean status; short rows

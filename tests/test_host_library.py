@@ -226,3 +226,16 @@ def test_decode_step_layout(pkv):
                                                                                  4096)
     assert pkv.lib().pkv_decode_step_layout(ctypes.byref(d), -1, 32, 256,
                                             ctypes.byref(lay)) == 1
+
+
+def test_auto_partition_is_a_multiple_of_four_chunks():
+    """The library's split-KV partition size, in 16-token chunks, is a multiple of 4 (one
+    chunk per warp per step, and whole 32-token blocks) and at least 8, over a grid of
+    batch shapes; in 32-token blocks it is half that."""
+    import itertools
+    import paged_kv_cache_58_gb300 as pkv
+    for s, hq, ctx in itertools.product([1, 2, 3, 7, 16, 64, 256, 4096], [1, 8, 32, 64],
+                                        [1, 17, 1000, 4096, 70000, 73728, 131072, 1 << 20]):
+        pc = pkv.auto_partition(s, hq, ctx, block_size=16)
+        assert pc % 4 == 0 and pc >= 8, (s, hq, ctx, pc)
+        assert pkv.auto_partition(s, hq, ctx, block_size=32) * 2 == pc
