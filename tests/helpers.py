@@ -32,11 +32,14 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 #  - the RMS error over the test within RMS_RATIO times the RMS error of the oracle's
 #    result rounded to the output dtype (what a kernel with no error of its own would
 #    show), plus 1e-5 of the RMS of the result for fp32 outputs, whose rounding is far
-#    below the fp32 accumulation error.
+#    below the fp32 accumulation error.  Measured on GB300 over the whole GPU suite:
+#    at most 1.02 on the decode and hi + lo prefill paths (their own error is ~2^-14 of
+#    the weights), at most 1.42 where one bf16 P per weight is kept; with 2.0 there, a
+#    kernel whose own error doubled (sqrt(1 + 2^2) = 2.24) fails.
 REL_FLOORED = 5e-3
 REL_FLOORED_SINGLE_P = 8e-3
-RMS_RATIO = 1.25
-RMS_RATIO_SINGLE_P = 4.0
+RMS_RATIO = 1.1
+RMS_RATIO_SINGLE_P = 2.0
 
 
 def _round_like(ref: np.ndarray, dtype) -> np.ndarray:
