@@ -111,6 +111,9 @@ pkv_status pkv_kv_append(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
  *                 ceil(context_len / block_size) are never read.
  *   context_lens  device int32 [num_seqs], each in [1, max_blocks_per_seq * block_size]
  *                 (the token being decoded is included: write it with kv_append first).
+ *                 A length below 1 raises PKV_ERR_INVALID in the device status word and
+ *                 gives that sequence's output rows zeros; a length above the range
+ *                 raises PKV_ERR_OOB and is clamped to it.
  *   max_context   host upper bound of context_lens (sizes the grid and workspace).
  *   scale         softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
  *   partition_blocks  blocks per split-KV partition; 0 lets the library choose.
@@ -228,7 +231,10 @@ pkv_status pkv_paged_decode_noalloc(const pkv_pool_desc* pool, void* out, const 
  *   prefix_len     > 0, a multiple of block_size; context_lens[s] >= prefix_len.
  *   max_context    host upper bound of context_lens (>= prefix_len).
  *   workspace      >= pkv_paged_decode_cascade_workspace_bytes(...) bytes, 16-byte aligned.
- * Other arguments as pkv_paged_decode.  Requires PKV_BF16. */
+ * Other arguments as pkv_paged_decode.  Requires PKV_BF16.  The prefix pass runs on a
+ * library-owned stream forked from `stream`; every return, errors included, first makes
+ * `stream` wait for it, so no work of the call outlives its ordering on `stream` and a
+ * stream capture always ends with the fork joined. */
 size_t pkv_paged_decode_cascade_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
                                                 int prefix_len, int max_context, int block_size,
                                                 int partition_blocks);

@@ -135,6 +135,14 @@ int decode_test_stall() {
     return v != nullptr && std::strcmp(v, "1") == 0;
 }
 
+// PKV_TEST_CASCADE_SUFFIX_FAIL=1 makes the cascade decode report a failed suffix launch
+// (without launching it) after its prefix pass was forked onto the side stream, so that
+// tests reach that error path (read at each call; tests only).
+bool cascade_test_fail_suffix() {
+    const char* v = std::getenv("PKV_TEST_CASCADE_SUFFIX_FAIL");
+    return v != nullptr && std::strcmp(v, "1") == 0;
+}
+
 size_t decode_workspace(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
     if (max_parts <= 1) return 0;
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
@@ -616,6 +624,7 @@ pkv_status cascade_impl(const pkv_pool_desc* pool, void* out, const void* q, con
     a.no_pdl = 1;
     a.k_new = k_new;
     a.v_new = v_new;
+    if (cascade_test_fail_suffix()) return PKV_ERR_CUDA;   // test hook: the rejoin still runs
     e = decode_use_simt() ? pkv::launch_paged_decode(a, pool->dtype, pool->head_dim, group, st_)
                           : pkv::launch_paged_decode_tc(a, pool->head_dim, group, st_);
     if (e != cudaSuccess) return e == cudaErrorNotSupported ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;

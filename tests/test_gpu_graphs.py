@@ -160,3 +160,42 @@ def test_fused_cascade_graph_replay(pkv):
     torch.cuda.synchronize()
     assert pkv.read_device_status() == 0
     assert torch.equal(out_eager, out_graph)
+
+
+def test_cascade_error_after_fork_leaves_capture_joined(pkv, monkeypatch):
+    """A cascade call that fails after forking its prefix pass onto the library's side
+    stream (PKV_TEST_CASCADE_SUFFIX_FAIL=1: the suffix launch reports a failure) still
+    makes the caller's stream wait for the side stream before returning: under stream
+    capture the capture ends cleanly (an unjoined side stream would make ending it fail),
+    and outside capture the next calls on the stream are correct."""
+    wl = dataclasses.replace(synth.WORKLOADS["shared"], num_seqs=4, shared_prefix=64,
+                             num_blocks=256)
+    case = synth.build_case(wl, "cuda", lengths=[5, 33, 1, 70], seed=41)
+    pkv.kv_append(case.k_pool, case.v_pool, case.slot_mapping, case.k_new, case.v_new)
+    prefix_blocks = case.block_tables[0, :4].contiguous()
+    max_ctx = case.max_context
+
+    def casc():
+        return pkv.paged_decode_cascade(case.q, case.k_pool, case.v_pool, prefix_blocks, 64,
+                                        case.block_tables, case.context_lens, case.scale,
+                                        max_context=max_ctx)
+
+    ref = casc()   # outside capture first: status word and side stream exist
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    monkeypatch.setenv("PKV_TEST_CASCADE_SUFFIX_FAIL", "1")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(pkv.PkvError) as e:
+        with torch.cuda.graph(g, stream=s):
+            casc()
+    assert e.value.status == 3
+    torch.cuda.current_stream().wait_stream(s)
+    with pytest.raises(pkv.PkvError):
+        casc()   # eager: fails the same way, joined before it returns
+    monkeypatch.delenv("PKV_TEST_CASCADE_SUFFIX_FAIL")
+    out = casc()
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
