@@ -65,10 +65,15 @@
 // (every barrier poll then costs a few hundred cycles), which is why the issue loops
 // are short and why one serial S/P ring left the pipe idle half the time.
 //
-// Warp roles (224 threads): warps 0-3 softmax + epilogue (warp w owns TMEM lanes
+// Warp roles (384 threads, three warpgroups): warps 0-3 softmax (warp w owns TMEM lanes
 // 32w..32w+31), warp 4 barrier set-up + TMA producer, warp 5 TMEM owner + stream-0
-// issuer, warp 6 stream-1 issuer.  TMEM columns: S/P buffers of streams 0 and 1 at [0, 128) and
-// [128, 256); their O at [256, 384) and [384, 512).
+// issuer, warp 6 stream-1 issuer, warp 7 idle, warps 8-11 epilogue (warp 8 + q reads
+// lanes 32q..32q+31).  At the end of an item the softmax warps hand the rows' merge
+// coefficients to the epilogue warps through shared memory and go on with the next
+// item; the epilogue warps wait for the last P.V products, read both accumulators out,
+// store the output and release the accumulators.  Registers (setmaxnreg): softmax 248 a
+// thread, producer and issuers 104, epilogue 152.  TMEM columns: S/P buffers of streams
+// 0 and 1 at [0, 128) and [128, 256); their O at [256, 384) and [384, 512).
 #include <atomic>
 #include <cstdlib>
 
@@ -89,7 +94,7 @@ constexpr int kChunk = 16;                 // tokens per staged chunk: a block, 
 constexpr int kHalf = kRows * 128;         // one 64-column half of the 128-row Q tile: 16 KB
 constexpr int kStagesK = 3;                // K stages: freed right after S = Q K^T
 constexpr int kStagesV = 3;                // V stages: freed after P.V
-constexpr int kNumBars = 24;
+constexpr int kNumBars = 26;
 
 constexpr int kMaxSchedReqs = 128;   // persistent scheduling ranks up to 128 requests
 
@@ -105,15 +110,25 @@ struct Geom {
     static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
     static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
-    // barriers, then the TMEM address and abort flag, then the persistent schedule
+    // barriers, then the TMEM address and abort flag, then the persistent schedule, then
+    // the per-row coefficients of the two streams' accumulators for the epilogue warps
     static constexpr int kOffSreq = kOffBar + kNumBars * 8 + 16;
     static constexpr int kOffOff = kOffSreq + kMaxSchedReqs * 2;
-    static constexpr int kSmemBytes = kOffOff + (kMaxSchedReqs + 1) * 4 + 1024;  // + align slack
+    static constexpr int kOffCoef = kOffOff + (kMaxSchedReqs + 1) * 4;
+    static constexpr int kSmemBytes = kOffCoef + 2 * kRows * 4 + 1024;  // + align slack
 };
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;                // issues stream 0 (even KV tiles); owns TMEM
-constexpr int kThreads = 224;              // warp 6 issues stream 1 (odd KV tiles)
+constexpr int kEpilogueWarp = 8;           // warps 8-11: epilogue (warp 6 issues stream 1)
+constexpr int kThreads = 384;
+// Register split (setmaxnreg) of the three warpgroups: softmax, producer + issuers,
+// epilogue.  The sum over the 384 threads (128 x (248 + 104 + 152) = 64512) must not
+// exceed what the launch provides (384 x the kernel's register count); the launcher
+// checks it.
+constexpr int kRegsSoftmax = 248;
+constexpr int kRegsIssue = 104;
+constexpr int kRegsEpilogue = 152;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;           // O of stream s at kTmemO + 128 s
 constexpr float kLazyRescale = 8.0f;       // log2 units
@@ -121,10 +136,22 @@ constexpr float kNoMax = -1.0e30f;         // running max before a stream saw a 
 
 // barrier indices: K/V stages (tile j uses stage j % 3), per-stream S/P buffer state.
 // BQ_EMPTY: every S of an item has run (the Q buffer may be reloaded); BO_FREE: per
-// stream, the softmax warps have read that stream's O out for an item.
+// stream, the epilogue warps have read that stream's O out for an item; BEPI: the
+// softmax warps have written an item's row coefficients; BCOEF_FREE: the epilogue warps
+// have read them.
 constexpr int BQ = 0, BK_FULL = 1, BK_EMPTY = 4, BV_FULL = 7, BV_EMPTY = 10, BS_FULL = 13,
               BP_FULL = 15, BPV_DONE = 17, BDRAIN = 19,   // BDRAIN: per stream, at exit
-              BQ_EMPTY = 21, BO_FREE = 22;
+              BQ_EMPTY = 21, BO_FREE = 22, BEPI = 24, BCOEF_FREE = 25;
+
+PKV_DEVINL void setmaxnreg_softmax() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+}
+PKV_DEVINL void setmaxnreg_issue() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
+}
+PKV_DEVINL void setmaxnreg_epilogue() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsEpilogue));
+}
 
 struct Ctl {
     uint64_t* bars;
@@ -334,8 +361,10 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (lane == 0) {
             mbar_init(&bars[BQ], 1);
             mbar_init(&bars[BQ_EMPTY], 2);
-            mbar_init(&bars[BO_FREE + 0], kSoftmaxWarps);
-            mbar_init(&bars[BO_FREE + 1], kSoftmaxWarps);
+            mbar_init(&bars[BO_FREE + 0], 4);   // the epilogue warps
+            mbar_init(&bars[BO_FREE + 1], 4);
+            mbar_init(&bars[BEPI], kSoftmaxWarps);
+            mbar_init(&bars[BCOEF_FREE], 4);
             for (int st = 0; st < kStagesK; ++st) {
                 mbar_init(&bars[BK_FULL + st], 1);
                 mbar_init(&bars[BK_EMPTY + st], 1);
@@ -367,6 +396,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t sK = smem_u32(smem + GM::kOffK);
     const uint32_t sV = smem_u32(smem + GM::kOffV);
 
+    if (warp >= kSoftmaxWarps && warp < kEpilogueWarp) {
+    setmaxnreg_issue();
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         // The whole warp runs the loop: each lane prefetches the block id of one 16-token
@@ -588,14 +619,87 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         // the TMEM is freed at the end of the kernel.
         umma_commit_if(leader, &bars[BDRAIN + sm]);
         mbar_wait_warp(&bars[BDRAIN + sm], 0, a.status);
+    }
+    } else if (warp >= kEpilogueWarp) {
+        setmaxnreg_epilogue();
+        // ------------------------------------------------------------ epilogue
+        // Warp 8 + q reads TMEM lanes 32 q .. 32 q + 31 (its lane quarter).  Per item with
+        // tiles: once the softmax warps have written the rows' coefficients (BEPI) and
+        // both streams' last P.V products are done, O = c_0 O_0 + c_1 O_1 is stored, and
+        // the accumulators and coefficients are released for the next item.  The same
+        // item list as every role; per stream, the parity of its tiles over all items.
+        const int q4 = warp & 3;
+        const int row = q4 * 32 + lane;   // == TMEM lane
+        const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
+        const float* coef = reinterpret_cast<const float*>(smem + GM::kOffCoef);
+        Cursor cur;
+        ItemParams p;
+        uint32_t par = 0;   // bit s: parity of stream s's tiles over all items
+        int e = 0;          // items ended
+        while (next_item<G>(a, sch, cur, false, p)) {
+            const int n0 = (p.ntiles + 1) >> 1, n1 = p.ntiles >> 1;   // tiles per stream
+            par ^= static_cast<uint32_t>(n0 & 1) | (static_cast<uint32_t>(n1 & 1) << 1);
+            bool fin = wait_bar_warp(ctl, BEPI, e & 1, lane);
+            if (fin) fin = wait_bar_warp(ctl, BPV_DONE + 0, (par & 1) ^ 1, lane);
+            if (fin && n1 > 0) fin = wait_bar_warp(ctl, BPV_DONE + 1, ((par >> 1) & 1) ^ 1, lane);
+            if (!fin) break;
+            tc_fence_after();
+            const float c0 = coef[row], c1 = coef[kRows + row];
+            const int tok = p.t0 + row / G;
+            const bool row_valid = tok < p.n;
+            const size_t orow_idx = static_cast<size_t>(p.qoff + tok) * a.num_q_heads +
+                                    p.kvh * G + row % G;
+            uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * D;
+            const size_t prow = orow_idx * a.max_parts_total + p.r;   // cascade: slot = split
+#pragma unroll
+            for (int q2 = 0; q2 < D / 32; ++q2) {
+                float o[32], o1[32];
+                tmem_ld32(tmem + lane_addr + kTmemO + q2 * 32, o);
+                if (n1 > 0) tmem_ld32(tmem + lane_addr + kTmemO + 128 + q2 * 32, o1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) o[k] *= c0;
+                if (n1 > 0) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = fmaf(o1[k], c1, o[k]);
+                }
+                if (cascade && row_valid) {
+                    float* dst = a.o_part + prow * D + q2 * 32;
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4)
+                        *reinterpret_cast<float4*>(dst + k) =
+                            make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+                } else if (row_valid) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 8) {
+                        uint4 w;
+                        w.x = pack_bf16x2(o[k], o[k + 1]);
+                        w.y = pack_bf16x2(o[k + 2], o[k + 3]);
+                        w.z = pack_bf16x2(o[k + 4], o[k + 5]);
+                        w.w = pack_bf16x2(o[k + 6], o[k + 7]);
+                        *reinterpret_cast<uint4*>(orow + q2 * 32 + k) = w;
+                    }
+                }
+            }
+            // O of this item and the coefficients are read: the issuers may start the next
+            // item's P.V products, the softmax warps may write the next coefficients.
+            tc_fence_before();
+            __syncwarp();
+            mbar_arrive_if(lane == 0, &bars[BO_FREE + 0]);
+            if (n1 > 0) mbar_arrive_if(lane == 0, &bars[BO_FREE + 1]);
+            mbar_arrive_if(lane == 0, &bars[BCOEF_FREE]);
+            ++e;
+        }
     } else {
-        // ------------------------------------------------------------ softmax + epilogue
+        setmaxnreg_softmax();
+        // ------------------------------------------------------------ softmax
         const int row = threadIdx.x;              // 0..127 == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
         const float sl2 = a.scale_log2;
         Cursor cur;
         ItemParams p;
         uint32_t par = 0;   // bit s: parity of stream s's tiles over all items
+        int ended = 0;      // items handed over to the epilogue warps
         bool ok = true;
         bool have = next_item<G>(a, sch, cur, false, p);
         while (ok && have) {
@@ -732,74 +836,35 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         if (!ok) break;
         // The next item's parameters, looked up now so that their loads overlap the
-        // epilogue's waits rather than delay the next item's first tile.
+        // hand-over below rather than delay the next item's first tile.
         ItemParams pn;
         const bool have_next = next_item<G>(a, sch, cur, false, pn);
-        // ------------------------------------------------------------ epilogue
+        // ------------------------------------------------------------ hand-over
         // Merge the streams: with a_s = 2^(m_s - m), m = max(m_0, m_1),
-        //   O = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1).
+        //   O = c_0 O_0 + c_1 O_1,  c_s = a_s / (a_0 l_0 + a_1 l_1).
         // Stream 0 always holds key 0, which every row sees, so m_0 and l_0 are proper.
-        const int n0 = (ntiles + 1) >> 1, n1 = ntiles >> 1;   // tiles of each stream
-        (void)n0;
-        bool fin = wait_bar_warp(ctl, BPV_DONE + 0, (par & 1) ^ 1, lane);
-        if (fin && n1 > 0) fin = wait_bar_warp(ctl, BPV_DONE + 1, ((par >> 1) & 1) ^ 1, lane);
-        if (!fin) break;
-        if (fin) {
-            tc_fence_after();
+        // The epilogue warps apply it once both streams' last P.V products are done; the
+        // softmax warps go on with the next item.  The coefficients of the previous item
+        // must have been read first (BCOEF_FREE).
+        {
+            const int n1 = ntiles >> 1;
+            if (ended >= 1 && !wait_bar_warp(ctl, BCOEF_FREE, (ended - 1) & 1, lane)) break;
             const float m = fmaxf(m_st[0], m_st[1]);
             const float a0 = fast_exp2(m_st[0] - m);
             const float a1 = n1 > 0 ? fast_exp2(m_st[1] - m) : 0.f;
             const float lsum = a0 * l_st[0] + a1 * l_st[1];
-            const float c0 = a0 / lsum, c1 = a1 / lsum;
-
-            uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * D;
-            const size_t prow = orow_idx * a.max_parts_total + prow_slot;   // cascade: slot = split
+            float* coef = reinterpret_cast<float*>(smem + GM::kOffCoef);
+            coef[row] = a0 / lsum;
+            coef[kRows + row] = a1 / lsum;
             if (cascade && row_valid) {
+                const size_t prow = orow_idx * a.max_parts_total + prow_slot;
                 a.m_part[prow] = m;   // log2 domain, as the decode partials
                 a.l_part[prow] = lsum;
             }
-            // 32 columns of both accumulators per TMEM round trip
-#pragma unroll
-            for (int q2 = 0; q2 < D / 32; ++q2) {
-            float oo[1][32], o1[1][32];
-            tmem_ld32(tmem + lane_addr + kTmemO + q2 * 32, oo[0]);
-            if (n1 > 0) tmem_ld32(tmem + lane_addr + kTmemO + 128 + q2 * 32, o1[0]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int hh = 0; hh < 1; ++hh) {
-                const int q = q2 + hh;
-                float* o = oo[hh];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] *= c0;
-                if (n1 > 0) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = fmaf(o1[hh][e], c1, o[e]);
-                }
-                if (cascade && row_valid) {
-                    float* dst = a.o_part + prow * D + q * 32;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(dst + e) =
-                            make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-                } else if (row_valid) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(o[e], o[e + 1]);
-                        w.y = pack_bf16x2(o[e + 2], o[e + 3]);
-                        w.z = pack_bf16x2(o[e + 4], o[e + 5]);
-                        w.w = pack_bf16x2(o[e + 6], o[e + 7]);
-                        *reinterpret_cast<uint4*>(orow + q * 32 + e) = w;
-                    }
-                }
-            }
-            }
+            __syncwarp();
+            mbar_arrive_if(lane == 0, &bars[BEPI]);
+            ++ended;
         }
-        // O of this item is read out: the issuers may start the next item's P.V.
-        tc_fence_before();
-        __syncwarp();
-        mbar_arrive_if(lane == 0, &bars[BO_FREE + 0]);
-        if (n1 > 0) mbar_arrive_if(lane == 0, &bars[BO_FREE + 1]);
         p = pn;
         have = have_next;
         }
@@ -835,6 +900,26 @@ int sm_count() {
     return v;
 }
 
+// The register split is only safe when the launch gives the CTA at least the registers
+// the split hands out: 384 threads x the kernel's register count (ptxas).  Checked once
+// per kernel and device; a kernel built with fewer registers is not launched.
+template <typename K>
+bool register_split_fits(K kern) {
+    static std::atomic<int> ok_cached[64];   // 0 unknown, 1 fits, 2 does not
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    int v = ok_cached[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        cudaFuncAttributes attr{};
+        if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void*>(kern)) != cudaSuccess)
+            return false;
+        const int need = 128 * (kRegsSoftmax + kRegsIssue + kRegsEpilogue);
+        v = attr.numRegs * kThreads >= need ? 1 : 2;
+        ok_cached[dev].store(v, std::memory_order_relaxed);
+    }
+    return v == 1;
+}
+
 template <int D, int G>
 cudaError_t launch_g(const PrefillArgs& a, cudaStream_t stream) {
     using GM = Geom<D>;
@@ -847,6 +932,7 @@ cudaError_t launch_g(const PrefillArgs& a, cudaStream_t stream) {
     if (!pool_ok || !make_q_group_map(&mq, a.q, a.total_new, a.num_q_heads, D, G, kRows / G))
         return cudaErrorInvalidValue;
     auto kern = prefill_tcgen05_kernel<D, G>;
+    if (!register_split_fits(kern)) return cudaErrorNotSupported;
     cudaError_t e =
         set_smem_once(reinterpret_cast<const void*>(kern), GM::kSmemBytes);
     if (e != cudaSuccess) return e;
