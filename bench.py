@@ -445,7 +445,18 @@ def decode_cpu_baseline(case, bytes_all, tokens_all, budget_s=8.0):
                       "(sequence, kv head)"}
 
 
-def bench_decode_line(pkv, dev, name, steps, stream, peaks_, cascade=False, cpu=True):
+def with_block_size(wl, block_size):
+    """The workload recipe with `block_size`-token pool blocks (the pool keeps its byte
+    size); unchanged for 0 or the recipe's own size."""
+    import dataclasses
+    if not block_size or block_size == wl.block_size:
+        return wl
+    return dataclasses.replace(wl, name=f"{wl.name}_B{block_size}", block_size=block_size,
+                               num_blocks=wl.num_blocks * wl.block_size // block_size)
+
+
+def bench_decode_line(pkv, dev, name, steps, stream, peaks_, cascade=False, cpu=True,
+                      block_size=0):
     """One published decode workload through its fused call (append + decode, or the
     cascade decode with the append for the shared-prefix batch), timed per call with
     CUDA events; its GB/s on the unique bytes against the HBM roofline, the logical rate,
@@ -453,7 +464,7 @@ def bench_decode_line(pkv, dev, name, steps, stream, peaks_, cascade=False, cpu=
     import torch
     import synth
     hbm, _, kind = peaks_
-    case = synth.build_case(name, dev)
+    case = synth.build_case(with_block_size(synth.WORKLOADS[name], block_size), dev)
     S, Hq, D = case.q.shape
     B = case.k_pool.shape[2]
     decode_bytes, append_bytes, tokens, unique = workload_bytes(case)
@@ -765,13 +776,8 @@ def main():
         pkv_build.build()
     ranks.barrier()
 
-    wl = synth.WORKLOADS[args.workload]
-    if args.block_size and args.block_size != wl.block_size:
-        import dataclasses
-        wl = dataclasses.replace(wl, name=f"{wl.name}_B{args.block_size}",
-                                 block_size=args.block_size,
-                                 num_blocks=wl.num_blocks * wl.block_size // args.block_size)
-    case = synth.build_case(wl, dev)
+    case = synth.build_case(with_block_size(synth.WORKLOADS[args.workload], args.block_size),
+                            dev)
     S, Hq, D = case.q.shape
     B = case.k_pool.shape[2]
     decode_bytes, append_bytes, tokens, unique_bytes = workload_bytes(case)
@@ -954,10 +960,12 @@ def main():
     long_decode = cascade_line = None
     if not args.no_long_decode and args.workload != "70b":
         long_decode = bench_decode_line(pkv, dev, "70b", args.sub_steps, stream, pk,
-                                        cpu=not args.no_cpu_baseline)
+                                        cpu=not args.no_cpu_baseline,
+                                        block_size=args.block_size)
     if not args.no_cascade_line and not (args.workload == "shared" and cascade):
         cascade_line = bench_decode_line(pkv, dev, "shared", args.sub_steps, stream, pk,
-                                         cascade=True, cpu=not args.no_cpu_baseline)
+                                         cascade=True, cpu=not args.no_cpu_baseline,
+                                         block_size=args.block_size)
     dtype = {torch.bfloat16: "bf16", torch.float32: "f32"}[case.q.dtype]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
