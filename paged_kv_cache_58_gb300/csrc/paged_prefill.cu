@@ -11,14 +11,14 @@
 // query heads that share kv head `kvh` (rows token-major, heads inner), so every K/V
 // tile staged for it serves all G heads.  Per 128-key KV tile j:
 //   S_j = Q K_j^T  tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) into the TMEM
-//                  S/P buffer of stream j % 2
+//                  S/P buffer g % 3 (g: the tile's index over the CTA's items)
 //   softmax        4 warps, one thread per row: tcgen05.ld S_j, causal mask, exp2,
 //                  row sums in fp32; P_j is split into bf16 hi + lo parts (hi = P
 //                  truncated, lo = the remainder truncated: hi + lo within 2^-14 of P)
 //                  and stored back over S_j in the same TMEM buffer (hi in its first
 //                  64 columns, lo in the next 64)
 //   O += P_j V_j   two tcgen05.mma passes (A = P hi, then P lo, from TMEM; B = V_j
-//                  from shared memory) into the TMEM accumulator O of stream j % 2
+//                  from shared memory) into the item's TMEM accumulator O
 // The split keeps the probabilities near fp32 precision: a single bf16 P is off by up
 // to 2^-8 per weight, which rows attending only a few keys do not average away; with
 // the split every output is within 2^-14 * max|v| of the exact weights' result.  A
@@ -28,26 +28,29 @@
 // output has a standard deviation near 2^-8 / sqrt(3 n / e) for n keys, about 1.2e-4
 // at n = 1024), and the P.V pass takes 8 MMAs instead of 16.
 // The running max is updated lazily: O and l are rescaled only when a row's max
-// grows by more than 2^8, which keeps P <= 256 and leaves the result exact.
+// grows by more than 2^8, which keeps P <= 256 and leaves the result exact.  With a
+// single P, an item's tiles after its first take the exponentials against the running
+// max first and skip the max pass when every row sum stays below 2^8 (no row grew).
 //
-// Two streams.  Even and odd KV tiles are two independent online-softmax passes,
-// each with its own S/P buffer, O accumulator, running max and row sum, merged by a
-// log-sum-exp step after the last tile.  Within a stream the chain S_j -> softmax ->
-// P_j V_j -> S_{j+2} (which overwrites P_j) is serial; the streams interleave, so the
-// tensor pipe works on one while the other waits for its softmax, and the softmax
-// warps always find the next S ready.  One warp issues each stream (S_j, then P_j V_j,
-// then S_{j+2} once that P.V completed: MMAs with different accumulators are not
-// ordered against each other).  K and V stages (3 each) are released when their S and
-// P.V have run, so the gathers of later tiles are in flight.  Each 16-token chunk of
-// a tile (a 16-token block, or half of a 32-token one) arrives as ONE TMA box: at
-// head_dim 128 a 4-D box (the chunk's 16 rows x 256 B viewed as 2 row groups x 2 column
-// halves x 8 rows x 128 B, 128-byte swizzle), so a K/V tile lands as [8-key group]
-// [column half][8 rows][128 B]: a valid K-major operand (8-row atoms 2 KB apart) for S
-// and MN-major operand (column halves 1 KB apart) for P.V; at head_dim 64 a 16-row x
-// 64-column box, the tile one 64-column half with 8-row atoms 1 KB apart.  On the
-// tile holding the last key a query tile needs, the P.V product skips the 16-key steps
-// wholly past that key (P = 0 there), and the issuer zeroes the V rows of its last step
-// past it (they may hold NaN from unused slots) once V has landed.
+// Three S/P buffers, one accumulator.  KV tile g of the CTA (counted over its items) is
+// scored into TMEM S/P buffer g % 3; P_g goes back over S_g in the same buffer, and
+// O += P_g V_g accumulates into one O for the item, so S_{g+3} may overwrite the buffer
+// only once P_g V_g has run.  While the softmax works on tile g, the tensor pipe runs
+// P_{g-1} V_{g-1} and the S products of up to two tiles ahead, so the chain S -> softmax
+// -> P.V -> S of one buffer has two softmax passes to complete in.  One warp issues the
+// S products, another the P.V products: MMAs into different accumulators are not
+// ordered against each other, so each waits on the barriers of its own inputs.  K and
+// V stages (3 each, tile g in stage g % 3) are released when their S and P.V have run,
+// so the gathers of later tiles are in flight.  Each 16-token chunk of a tile (a
+// 16-token block, or half of a 32-token one) arrives as ONE TMA box: at head_dim 128 a
+// 4-D box (the chunk's 16 rows x 256 B viewed as 2 row groups x 2 column halves x 8
+// rows x 128 B, 128-byte swizzle), so a K/V tile lands as [8-key group][column half]
+// [8 rows][128 B]: a valid K-major operand (8-row atoms 2 KB apart) for S and MN-major
+// operand (column halves 1 KB apart) for P.V; at head_dim 64 a 16-row x 64-column box,
+// the tile one 64-column half with 8-row atoms 1 KB apart.  On the tile holding the
+// last key a query tile needs, the P.V product skips the 16-key steps wholly past that
+// key (P = 0 there), and the issuer zeroes the V rows of its last step past it (they
+// may hold NaN from unused slots) once V has landed.
 //
 // Persistent CTAs.  A CTA pays about 5 us outside its tile loop (barrier and TMEM set-up,
 // the first gathers and S, the epilogue), which nothing overlaps when each SM runs one
@@ -56,24 +59,25 @@
 // next item's Q, gathers and first S products under way while the softmax warps finish
 // the current one.
 //
-// Measured costs per 128-key tile on GB300 (clock64 traces and isolated probes): the
-// 24 N = 128 MMAs (8 for S, 16 for the hi + lo P.V) take the tensor pipe about 1700
-// cycles (64 each at full rate); the softmax of 128 rows about 1300 cycles on its four
-// warps.  The TMA producer spends about 100 cycles per box, so two 2 KB boxes per
-// block made it the bottleneck until one 4 KB box per block halved that.  A warp that
-// issues MMAs gets only the issue slots its scheduler's softmax warp leaves free
-// (every barrier poll then costs a few hundred cycles), which is why the issue loops
-// are short and why one serial S/P ring left the pipe idle half the time.
+// Measured costs per 128-key tile on GB300 (clock64 traces, isolated probes, and copies
+// of this kernel with parts of the work removed): the 16 N = 128 MMAs of a single-P
+// tile take the tensor pipe 1024 cycles (64 each at full rate), the softmax of 128 rows
+// about 1300 cycles on its four warps, and a warp issuing TMA boxes about 100 cycles per
+// box: with all 16 boxes of a tile from one warp the kernel took 0.372 ms on the 16 x
+// 512-token batch with no softmax work at all, with K and V from two warps 0.308 ms.
+// Shared memory serves about 160 KB a tile (S reads Q and K, P.V reads V, the copies
+// write K and V) at up to 128 B a cycle.  A warp that issues MMAs gets only the issue
+// slots its scheduler's softmax warp leaves free, which is why the issue loops are short.
 //
 // Warp roles (384 threads, three warpgroups): warps 0-3 softmax (warp w owns TMEM lanes
-// 32w..32w+31), warp 4 barrier set-up + TMA producer, warp 5 TMEM owner + stream-0
-// issuer, warp 6 stream-1 issuer, warp 7 idle, warps 8-11 epilogue (warp 8 + q reads
-// lanes 32q..32q+31).  At the end of an item the softmax warps hand the rows' merge
-// coefficients to the epilogue warps through shared memory and go on with the next
-// item; the epilogue warps wait for the last P.V products, read both accumulators out,
-// store the output and release the accumulators.  Registers (setmaxnreg): softmax 248 a
-// thread, producer and issuers 104, epilogue 152.  TMEM columns: S/P buffers of streams
-// 0 and 1 at [0, 128) and [128, 256); their O at [256, 384) and [384, 512).
+// 32w..32w+31), warp 4 barrier set-up + Q and K copies, warp 5 TMEM owner + S issuer,
+// warp 6 P.V issuer, warp 7 V copies, warps 8-11 epilogue (warp 8 + q reads lanes
+// 32q..32q+31).  At the end of an item the softmax warps hand the rows' 1 / l to the
+// epilogue warps through shared memory and go on with the next item; the epilogue warps
+// wait for the item's last P.V product, read the accumulator out, store the output and
+// release the accumulator.  Registers (setmaxnreg): softmax 248 a thread, copies and
+// issuers 104, epilogue 152.  TMEM columns: S/P buffers at [0, 128), [128, 256) and
+// [256, 384); O at [384, 384 + head_dim).
 #include <atomic>
 #include <cstdlib>
 
@@ -94,7 +98,7 @@ constexpr int kChunk = 16;                 // tokens per staged chunk: a block, 
 constexpr int kHalf = kRows * 128;         // one 64-column half of the 128-row Q tile: 16 KB
 constexpr int kStagesK = 3;                // K stages: freed right after S = Q K^T
 constexpr int kStagesV = 3;                // V stages: freed after P.V
-constexpr int kNumBars = 26;
+constexpr int kNumBars = 28;
 
 constexpr int kMaxSchedReqs = 128;   // persistent scheduling ranks up to 128 requests
 
@@ -111,16 +115,18 @@ struct Geom {
     static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
     static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
     // barriers, then the TMEM address and abort flag, then the persistent schedule, then
-    // the per-row coefficients of the two streams' accumulators for the epilogue warps
+    // the rows' 1 / l for the epilogue warps
     static constexpr int kOffSreq = kOffBar + kNumBars * 8 + 16;
     static constexpr int kOffOff = kOffSreq + kMaxSchedReqs * 2;
     static constexpr int kOffCoef = kOffOff + (kMaxSchedReqs + 1) * 4;
-    static constexpr int kSmemBytes = kOffCoef + 2 * kRows * 4 + 1024;  // + align slack
+    static constexpr int kSmemBytes = kOffCoef + kRows * 4 + 1024;  // + align slack
 };
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;                // issues stream 0 (even KV tiles); owns TMEM
-constexpr int kEpilogueWarp = 8;           // warps 8-11: epilogue (warp 6 issues stream 1)
+constexpr int kMmaWarp = 5;                // issues the S products; owns TMEM
+constexpr int kPvWarp = 6;                 // issues the P.V products
+constexpr int kProducerVWarp = 7;          // V copies (warp 4: Q and K copies)
+constexpr int kEpilogueWarp = 8;           // warps 8-11: epilogue
 constexpr int kThreads = 384;
 // Register split (setmaxnreg) of the three warpgroups: softmax, producer + issuers,
 // epilogue.  The sum over the 384 threads (128 x (248 + 104 + 152) = 64512) must not
@@ -130,18 +136,21 @@ constexpr int kRegsSoftmax = 248;
 constexpr int kRegsIssue = 104;
 constexpr int kRegsEpilogue = 152;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;           // O of stream s at kTmemO + 128 s
+constexpr int kSBufs = 3;                  // S/P buffers; buffer b at TMEM column 128 b
+constexpr uint32_t kTmemO = 384;           // the O accumulator
+static_assert(kStagesK == kSBufs && kStagesV == kSBufs, "tile g uses stage and buffer g % 3");
 constexpr float kLazyRescale = 8.0f;       // log2 units
-constexpr float kNoMax = -1.0e30f;         // running max before a stream saw a key
+constexpr float kLazyLimit = 256.0f;       // 2^kLazyRescale
+constexpr float kNoMax = -1.0e30f;         // running max before an item's first tile
 
-// barrier indices: K/V stages (tile j uses stage j % 3), per-stream S/P buffer state.
-// BQ_EMPTY: every S of an item has run (the Q buffer may be reloaded); BO_FREE: per
-// stream, the epilogue warps have read that stream's O out for an item; BEPI: the
-// softmax warps have written an item's row coefficients; BCOEF_FREE: the epilogue warps
-// have read them.
+// barrier indices: K/V stages and S/P buffers (the CTA's tile g uses stage and buffer
+// g % 3).  BQ_EMPTY: every S of an item has run (the Q buffer may be reloaded); BO_FREE:
+// the epilogue warps have read O out for an item; BEPI: the softmax warps have written an
+// item's row coefficients; BCOEF_FREE: the epilogue warps have read them; BDRAIN: per
+// issuing warp, at exit.
 constexpr int BQ = 0, BK_FULL = 1, BK_EMPTY = 4, BV_FULL = 7, BV_EMPTY = 10, BS_FULL = 13,
-              BP_FULL = 15, BPV_DONE = 17, BDRAIN = 19,   // BDRAIN: per stream, at exit
-              BQ_EMPTY = 21, BO_FREE = 22, BEPI = 24, BCOEF_FREE = 25;
+              BP_FULL = 16, BPV_DONE = 19, BDRAIN = 22, BQ_EMPTY = 24, BO_FREE = 25,
+              BEPI = 26, BCOEF_FREE = 27;
 
 PKV_DEVINL void setmaxnreg_softmax() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
@@ -360,23 +369,21 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (warp == kProducerWarp) {
         if (lane == 0) {
             mbar_init(&bars[BQ], 1);
-            mbar_init(&bars[BQ_EMPTY], 2);
-            mbar_init(&bars[BO_FREE + 0], 4);   // the epilogue warps
-            mbar_init(&bars[BO_FREE + 1], 4);
+            mbar_init(&bars[BQ_EMPTY], 1);
+            mbar_init(&bars[BO_FREE], 4);   // the epilogue warps
             mbar_init(&bars[BEPI], kSoftmaxWarps);
             mbar_init(&bars[BCOEF_FREE], 4);
-            for (int st = 0; st < kStagesK; ++st) {
+            for (int st = 0; st < kSBufs; ++st) {
                 mbar_init(&bars[BK_FULL + st], 1);
                 mbar_init(&bars[BK_EMPTY + st], 1);
                 mbar_init(&bars[BV_FULL + st], 1);
                 mbar_init(&bars[BV_EMPTY + st], 1);
+                mbar_init(&bars[BS_FULL + st], 1);
+                mbar_init(&bars[BP_FULL + st], kSoftmaxWarps);
+                mbar_init(&bars[BPV_DONE + st], 1);
             }
-            for (int sm = 0; sm < 2; ++sm) {
-                mbar_init(&bars[BS_FULL + sm], 1);
-                mbar_init(&bars[BP_FULL + sm], kSoftmaxWarps);
-                mbar_init(&bars[BPV_DONE + sm], 1);
-                mbar_init(&bars[BDRAIN + sm], 1);
-            }
+            mbar_init(&bars[BDRAIN + 0], 1);
+            mbar_init(&bars[BDRAIN + 1], 1);
             *abort_flag = 0;
             fence_mbar_init();
             prefetch_tmap(&tm_q);
@@ -398,14 +405,18 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     if (warp >= kSoftmaxWarps && warp < kEpilogueWarp) {
     setmaxnreg_issue();
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ TMA producer
-        // The whole warp runs the loop: each lane prefetches the block id of one 16-token
-        // chunk (32 chunks = 4 KV tiles per refill, independent loads), lane 0 sets the
-        // byte counts and lane b < 8 issues the box of chunk b of the tile.  A chunk is
-        // a whole block (block size 16) or rows 16 h .. 16 h + 15 of one (block size 32).
-        // Stages and their phases count the CTA's tiles over all its items (g); the Q of
-        // an item is loaded once every S product of the previous item has run.
+    if (warp == kProducerWarp || warp == kProducerVWarp) {
+        // ------------------------------------------------------------ TMA producers
+        // Warp 4 copies Q and K, warp 7 V: a warp spends about 100 cycles per box it
+        // issues, and one warp issuing both K and V (16 boxes per KV tile) set the pace of
+        // the whole kernel.  Each warp runs the loop whole: each lane prefetches the block
+        // id of one 16-token chunk (32 chunks = 4 KV tiles per refill, independent loads),
+        // lane 0 sets the byte counts and lane b < 8 issues the box of chunk b of the
+        // tile.  A chunk is a whole block (block size 16) or rows 16 h .. 16 h + 15 of one
+        // (block size 32).  Stages and their phases count the CTA's tiles over all its
+        // items (g); the Q of an item is loaded once every S product of the previous item
+        // has run.
+        const bool doqk = warp == kProducerWarp;
         Cursor cur;
         ItemParams p;
         int it = 0, g = 0;
@@ -415,13 +426,13 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int32_t* bt =
                 a.block_tables + static_cast<size_t>(cascade ? 0 : p.r) * a.max_blocks_per_seq;
             const int nchunks = p.max_lim / kChunk + 1;
-            if (it >= 1 && !wait_bar_warp(ctl, BQ_EMPTY, (it - 1) & 1, lane)) break;
+            if (doqk && it >= 1 && !wait_bar_warp(ctl, BQ_EMPTY, (it - 1) & 1, lane)) break;
             // Test hook (zero in normal use): CTA 0 arms its first Q barrier for 16 bytes
             // more than the Q copy delivers, so the issuers' wait for it runs out of time
             // (PKV_ERR_TIMEOUT) while the copy still lands.
             const bool stall = test_stall && it == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
                                blockIdx.z == 0;
-            if (lane == 0) {
+            if (doqk && lane == 0) {
                 mbar_arrive_expect_tx(&bars[BQ], GM::kQBytes + (stall ? 16u : 0u));
 #pragma unroll
                 for (int h = 0; h < GM::kHalves; ++h)
@@ -450,41 +461,41 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // K of tile g: its stage is free once S of tile g - kStagesK has run.  The
                 // warp stays converged: lane 0 sets the byte count and lanes b < nb issue
                 // the boxes through predicated instructions.
-                if (g >= kStagesK &&
+                if (doqk && g >= kStagesK &&
                     !wait_bar_warp(ctl, BK_EMPTY + sk, ((g / kStagesK) - 1) & 1, lane)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx_if(lane == 0, &bars[BK_FULL + sk], nb * GM::kChunkBytes);
+                mbar_arrive_expect_tx_if(doqk && lane == 0, &bars[BK_FULL + sk], nb * GM::kChunkBytes);
                 {
                     uint8_t* dst = smem + GM::kOffK + sk * GM::kTileBytes + lane * GM::kChunkBytes;
                     if constexpr (D == 128)
-                        tma_load_4d_if(lane < nb, dst, &tm_k, 0, 0, 0, row / 8, &bars[BK_FULL + sk]);
+                        tma_load_4d_if(doqk && lane < nb, dst, &tm_k, 0, 0, 0, row / 8, &bars[BK_FULL + sk]);
                     else
-                        tma_load_2d_if(lane < nb, dst, &tm_k, 0, row, &bars[BK_FULL + sk]);
+                        tma_load_2d_if(doqk && lane < nb, dst, &tm_k, 0, row, &bars[BK_FULL + sk]);
                 }
-                ++k_issued;
+                k_issued += doqk;
                 // V of tile g: its stage is free once P.V of tile g - kStagesV has run.
-                if (g >= kStagesV &&
+                if (!doqk && g >= kStagesV &&
                     !wait_bar_warp(ctl, BV_EMPTY + sv, ((g / kStagesV) - 1) & 1, lane)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx_if(lane == 0, &bars[BV_FULL + sv], nb * GM::kChunkBytes);
+                mbar_arrive_expect_tx_if(!doqk && lane == 0, &bars[BV_FULL + sv], nb * GM::kChunkBytes);
                 {
                     uint8_t* dst = smem + GM::kOffV + sv * GM::kTileBytes + lane * GM::kChunkBytes;
                     if constexpr (D == 128)
-                        tma_load_4d_if(lane < nb, dst, &tm_v, 0, 0, 0, row / 8, &bars[BV_FULL + sv]);
+                        tma_load_4d_if(!doqk && lane < nb, dst, &tm_v, 0, 0, 0, row / 8, &bars[BV_FULL + sv]);
                     else
-                        tma_load_2d_if(lane < nb, dst, &tm_v, 0, row, &bars[BV_FULL + sv]);
+                        tma_load_2d_if(!doqk && lane < nb, dst, &tm_v, 0, row, &bars[BV_FULL + sv]);
                 }
-                ++v_issued;
+                v_issued += !doqk;
             }
         }
         // Drain (also after an abort): wait, bounded, until the last copy issued into
         // every stage has landed, so that no TMA write into shared memory outlives the
         // CTA.  No later copy goes into those stages, so the phases cannot move on.
-        if (it >= 1) mbar_wait_warp(&bars[BQ], (it - 1) & 1, a.status);
+        if (doqk && it >= 1) mbar_wait_warp(&bars[BQ], (it - 1) & 1, a.status);
         for (int st = 0; st < kStagesK; ++st) {
             if (k_issued > st) {
                 const int last = st + kStagesK * ((k_issued - 1 - st) / kStagesK);
@@ -495,82 +506,87 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 mbar_wait_warp(&bars[BV_FULL + st], (last / kStagesV) & 1, a.status);
             }
         }
-    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-        // ------------------------------------------------------------ MMA issuers
-        // Stream sm = warp - kMmaWarp owns an item's KV tiles j = sm, sm + 2, ...: S_j into
-        // its S/P buffer, then O_sm += P_j V_j once the softmax has written P_j there, then
-        // S_{j+2} into the same buffer once that P.V has completed.  Each stream is a
-        // serial chain, but the two interleave in the tensor pipe.  Each issuing warp
-        // shares its scheduler with a softmax warp and gets only the issue slots that
-        // warp leaves free, so the loop is short: the whole warp runs it converged (all
-        // lanes poll, then one leader lane issues through predicated instructions), and
-        // the descriptors are precomputed halves plus constant offsets.  Across items:
-        // an item's first P.V into O_sm waits until the softmax warps have read O_sm out
-        // for the last item in which this stream had tiles (BO_FREE + sm, one phase per
-        // such item), and once this stream's last S of an item has run it signals that
-        // the Q buffer may take the next item's Q (BQ_EMPTY; a stream without tiles in
-        // the item just arrives).  Both issuers wait for every phase of BQ, tiles or not,
-        // so that no parity wait can fall two phases behind.
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ S issuer
+        // S_g = Q K_g^T into S/P buffer g % 3 once K_g has landed and the buffer's
+        // previous tile g - 3 has been consumed by its P.V product (P_{g-3} lies in the
+        // same columns); at an item's first tile, once the item's Q has landed.  After an
+        // item's last S it signals that the Q buffer may take the next item's Q
+        // (BQ_EMPTY).  The issuing warps share their schedulers with softmax warps and
+        // get only the issue slots those leave free, so the loops are short: the whole
+        // warp runs them converged (all lanes poll, one leader lane issues through
+        // predicated instructions) and the descriptors are precomputed halves plus
+        // constant offsets.
         constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, kKeys, false, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, D, false, true);
         constexpr uint32_t hi_q = smem_desc_sw128_hi(1024);          // Q: 8-row atoms 1 KB apart
-        constexpr uint32_t hi_kv = smem_desc_sw128_hi(GM::kGroupBytes);  // K/V: 8-key groups
-        const int sm = warp - kMmaWarp;
+        constexpr uint32_t hi_kv = smem_desc_sw128_hi(GM::kGroupBytes);  // K: 8-key groups
         const uint32_t lo_q = smem_desc_sw128_lo(sQ, 16);
         const uint32_t lo_k = smem_desc_sw128_lo(sK, 16);
-        const uint32_t lo_v = smem_desc_sw128_lo(sV, 1024);          // V: column halves 1 KB apart
-        const uint32_t tS = tmem + sm * 128;
-        const uint32_t tO = tmem + kTmemO + sm * 128;
-        const bool leader = elect_one();   // issues every MMA and commit of this stream
+        const bool leader = elect_one();   // issues every MMA and commit of this warp
         Cursor cur;
         ItemParams p;
-        int it = 0, g0 = 0;
-        uint32_t use = 0;     // this stream's tiles over all items (S/P buffer phases)
-        uint32_t o_use = 0;   // items in which this stream had tiles (O_sm read-outs)
+        int it = 0, g = 0;
         bool ok = true;
         while (ok && next_item<G>(a, sch, cur, false, p)) {
             ok = wait_bar_warp(ctl, BQ, it & 1, lane);
-            bool o_free = o_use == 0;   // O_sm read out after its last item
-            for (int j = sm; ok && j < p.ntiles; j += 2, ++use) {
-                const int g = g0 + j;
-                const int st = g % kStagesK;
-                // S_j: K_j landed, and P of this buffer's previous tile consumed by its P.V.
-                if (!wait_bar_warp(ctl, BK_FULL + st, (g / kStagesK) & 1, lane)) { ok = false; break; }
-                if (use >= 1 && !wait_bar_warp(ctl, BPV_DONE + sm, (use - 1) & 1, lane)) {
+            for (int j = 0; ok && j < p.ntiles; ++j, ++g) {
+                const int b = g % kSBufs;
+                if (!wait_bar_warp(ctl, BK_FULL + b, (g / kSBufs) & 1, lane)) { ok = false; break; }
+                if (g >= kSBufs &&
+                    !wait_bar_warp(ctl, BPV_DONE + b, ((g / kSBufs) - 1) & 1, lane)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                {
-                    const uint32_t lk = lo_k + ((st * GM::kTileBytes) >> 4);
+                const uint32_t tS = tmem + b * 128;
+                const uint32_t lk = lo_k + ((b * GM::kTileBytes) >> 4);
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t kc = ((ks & 3) * 32) >> 4;   // 16 columns = 32 B
-                        umma_bf16_if(leader, tS,
-                                     desc_join(lo_q + (((ks >> 2) * kHalf) >> 4) + kc, hi_q),
-                                     desc_join(lk + (((ks >> 2) * 1024) >> 4) + kc, hi_kv),
-                                     idesc_qk, ks > 0);
-                    }
-                    umma_commit_if(leader, &bars[BS_FULL + sm]);
-                    umma_commit_if(leader, &bars[BK_EMPTY + st]);
-                    if (j + 2 >= p.ntiles) umma_commit_if(leader, &bars[BQ_EMPTY]);   // last S
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t kc = ((ks & 3) * 32) >> 4;   // 16 columns = 32 B
+                    umma_bf16_if(leader, tS,
+                                 desc_join(lo_q + (((ks >> 2) * kHalf) >> 4) + kc, hi_q),
+                                 desc_join(lk + (((ks >> 2) * 1024) >> 4) + kc, hi_kv),
+                                 idesc_qk, ks > 0);
                 }
-                // O_sm += P_j V_j: P_j written, V_j landed, O_sm read out (first tile).
-                const int sv = g % kStagesV;
-                if (!wait_bar_warp(ctl, BP_FULL + sm, use & 1, lane)) { ok = false; break; }
-                if (!wait_bar_warp(ctl, BV_FULL + sv, (g / kStagesV) & 1, lane)) { ok = false; break; }
-                if (!o_free) {
-                    if (!wait_bar_warp(ctl, BO_FREE + sm, (o_use - 1) & 1, lane)) {
-                        ok = false;
-                        break;
-                    }
-                    o_free = true;
+                umma_commit_if(leader, &bars[BS_FULL + b]);
+                umma_commit_if(leader, &bars[BK_EMPTY + b]);
+                if (j + 1 == p.ntiles) umma_commit_if(leader, &bars[BQ_EMPTY]);   // last S
+            }
+            ++it;
+        }
+        // Drain (also after an abort): every MMA this warp issued completes before the
+        // TMEM is freed at the end of the kernel.
+        umma_commit_if(leader, &bars[BDRAIN + 0]);
+        mbar_wait_warp(&bars[BDRAIN + 0], 0, a.status);
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------ P.V issuer
+        // O += P_g V_g once the softmax warps have written P_g into buffer g % 3 and V_g
+        // has landed; an item's first P.V overwrites O, once the epilogue warps have read
+        // the previous item's O out (BO_FREE).  The P.V products all accumulate into the
+        // one O and run in issue order.
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, D, false, true);
+        constexpr uint32_t hi_kv = smem_desc_sw128_hi(GM::kGroupBytes);  // V: 8-key groups
+        const uint32_t lo_v = smem_desc_sw128_lo(sV, 1024);          // V: column halves 1 KB apart
+        const uint32_t tO = tmem + kTmemO;
+        const bool leader = elect_one();
+        Cursor cur;
+        ItemParams p;
+        int it = 0, g = 0;
+        bool ok = true;
+        while (ok && next_item<G>(a, sch, cur, false, p)) {
+            for (int j = 0; ok && j < p.ntiles; ++j, ++g) {
+                const int b = g % kSBufs;
+                if (!wait_bar_warp(ctl, BP_FULL + b, (g / kSBufs) & 1, lane)) { ok = false; break; }
+                if (!wait_bar_warp(ctl, BV_FULL + b, (g / kSBufs) & 1, lane)) { ok = false; break; }
+                if (j == 0 && it >= 1 && !wait_bar_warp(ctl, BO_FREE, (it - 1) & 1, lane)) {
+                    ok = false;
+                    break;
                 }
                 // Keys past the last one this tile needs are masked for every row (P = 0),
                 // but their V rows may hold anything (NaN in unused slots, stale data where
                 // no block was loaded this tile).  The P.V product skips the 16-key steps
                 // that lie wholly past that key, and the rows of the last step past it are
-                // zeroed, now that V_j has landed, so that 0 * V stays 0.
+                // zeroed, now that V_g has landed, so that 0 * V stays 0.
                 const int kbase = (p.j0 + j) * kKeys;
                 const int nvalid = min(kKeys, p.max_lim - kbase + 1);   // >= 1
                 const int ksteps = (nvalid + 15) >> 4;
@@ -583,7 +599,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const int row = nvalid + t / (8 * GM::kHalves);
                         const int hh = (t / 8) % GM::kHalves;
                         const int jj = t & 7;
-                        uint8_t* vrow = smem + GM::kOffV + sv * GM::kTileBytes +
+                        uint8_t* vrow = smem + GM::kOffV + b * GM::kTileBytes +
                                         (row >> 3) * GM::kGroupBytes + (row & 7) * 128;
                         *reinterpret_cast<uint4*>(vrow + hh * 1024 + ((jj ^ (row & 7)) << 4)) = z;
                     }
@@ -591,60 +607,49 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                     __syncwarp();
                 }
                 tc_fence_after();
-                {
-                    const uint32_t lv = lo_v + ((sv * GM::kTileBytes) >> 4);
-                    // V as the MN-major B operand: 16 keys = two 8-key groups.
+                const uint32_t tS = tmem + b * 128;
+                const uint32_t lv = lo_v + ((b * GM::kTileBytes) >> 4);
+                // V as the MN-major B operand: 16 keys = two 8-key groups.
 #pragma unroll
-                    for (int ks = 0; ks < kKeys / 16; ++ks) {
-                        const uint64_t bv = desc_join(lv + ((ks * 2 * GM::kGroupBytes) >> 4), hi_kv);
-                        umma_bf16_ta_if(leader && ks < ksteps, tO, tS + ks * 8, bv, idesc_pv,
-                                        (j >= 2) || (ks > 0));
-                        if (!p.p_single)
-                            umma_bf16_ta_if(leader && ks < ksteps, tO, tS + 64 + ks * 8, bv,
-                                            idesc_pv, true);
-                    }
-                    umma_commit_if(leader, &bars[BPV_DONE + sm]);
-                    umma_commit_if(leader, &bars[BV_EMPTY + sv]);
+                for (int ks = 0; ks < kKeys / 16; ++ks) {
+                    const uint64_t bv = desc_join(lv + ((ks * 2 * GM::kGroupBytes) >> 4), hi_kv);
+                    umma_bf16_ta_if(leader && ks < ksteps, tO, tS + ks * 8, bv, idesc_pv,
+                                    (j > 0) || (ks > 0));
+                    if (!p.p_single)
+                        umma_bf16_ta_if(leader && ks < ksteps, tO, tS + 64 + ks * 8, bv,
+                                        idesc_pv, true);
                 }
+                umma_commit_if(leader, &bars[BPV_DONE + b]);
+                umma_commit_if(leader, &bars[BV_EMPTY + b]);
             }
-            if (!ok) break;
-            if (sm >= p.ntiles)
-                mbar_arrive_if(leader, &bars[BQ_EMPTY]);   // no S in this item
-            else
-                ++o_use;
-            g0 += p.ntiles;
             ++it;
         }
-        // Drain (also after an abort): every MMA this stream issued completes before
-        // the TMEM is freed at the end of the kernel.
-        umma_commit_if(leader, &bars[BDRAIN + sm]);
-        mbar_wait_warp(&bars[BDRAIN + sm], 0, a.status);
+        umma_commit_if(leader, &bars[BDRAIN + 1]);
+        mbar_wait_warp(&bars[BDRAIN + 1], 0, a.status);
     }
     } else if (warp >= kEpilogueWarp) {
         setmaxnreg_epilogue();
         // ------------------------------------------------------------ epilogue
-        // Warp 8 + q reads TMEM lanes 32 q .. 32 q + 31 (its lane quarter).  Per item with
-        // tiles: once the softmax warps have written the rows' coefficients (BEPI) and
-        // both streams' last P.V products are done, O = c_0 O_0 + c_1 O_1 is stored, and
-        // the accumulators and coefficients are released for the next item.  The same
-        // item list as every role; per stream, the parity of its tiles over all items.
+        // Warp 8 + q reads TMEM lanes 32 q .. 32 q + 31 (its lane quarter).  Per item: once
+        // the softmax warps have written the rows' coefficients 1 / l (BEPI) and the
+        // item's last P.V product is done, O / l is stored, and the accumulator and the
+        // coefficients are released for the next item.  The same item list as every role.
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;   // == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
         const float* coef = reinterpret_cast<const float*>(smem + GM::kOffCoef);
         Cursor cur;
         ItemParams p;
-        uint32_t par = 0;   // bit s: parity of stream s's tiles over all items
-        int e = 0;          // items ended
+        int e = 0;   // items ended
+        int g = 0;   // the CTA's tiles over all items
         while (next_item<G>(a, sch, cur, false, p)) {
-            const int n0 = (p.ntiles + 1) >> 1, n1 = p.ntiles >> 1;   // tiles per stream
-            par ^= static_cast<uint32_t>(n0 & 1) | (static_cast<uint32_t>(n1 & 1) << 1);
+            g += p.ntiles;
+            const int gl = g - 1;   // the item's last tile
             bool fin = wait_bar_warp(ctl, BEPI, e & 1, lane);
-            if (fin) fin = wait_bar_warp(ctl, BPV_DONE + 0, (par & 1) ^ 1, lane);
-            if (fin && n1 > 0) fin = wait_bar_warp(ctl, BPV_DONE + 1, ((par >> 1) & 1) ^ 1, lane);
+            if (fin) fin = wait_bar_warp(ctl, BPV_DONE + gl % kSBufs, (gl / kSBufs) & 1, lane);
             if (!fin) break;
             tc_fence_after();
-            const float c0 = coef[row], c1 = coef[kRows + row];
+            const float c = coef[row];
             const int tok = p.t0 + row / G;
             const bool row_valid = tok < p.n;
             const size_t orow_idx = static_cast<size_t>(p.qoff + tok) * a.num_q_heads +
@@ -652,41 +657,38 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * D;
             const size_t prow = orow_idx * a.max_parts_total + p.r;   // cascade: slot = split
 #pragma unroll
-            for (int q2 = 0; q2 < D / 32; ++q2) {
-                float o[32], o1[32];
-                tmem_ld32(tmem + lane_addr + kTmemO + q2 * 32, o);
-                if (n1 > 0) tmem_ld32(tmem + lane_addr + kTmemO + 128 + q2 * 32, o1);
+            for (int q2 = 0; q2 < D / 64; ++q2) {
+                float o[64];
+                tmem_ld32(tmem + lane_addr + kTmemO + q2 * 64,
+                          *reinterpret_cast<float(*)[32]>(&o[0]));
+                tmem_ld32(tmem + lane_addr + kTmemO + q2 * 64 + 32,
+                          *reinterpret_cast<float(*)[32]>(&o[32]));
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 32; ++k) o[k] *= c0;
-                if (n1 > 0) {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = fmaf(o1[k], c1, o[k]);
-                }
+                for (int k = 0; k < 64; ++k) o[k] *= c;
                 if (cascade && row_valid) {
-                    float* dst = a.o_part + prow * D + q2 * 32;
+                    float* dst = a.o_part + prow * D + q2 * 64;
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4)
+                    for (int k = 0; k < 64; k += 4)
                         *reinterpret_cast<float4*>(dst + k) =
                             make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
                 } else if (row_valid) {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 8) {
+                    for (int k = 0; k < 64; k += 8) {
                         uint4 w;
                         w.x = pack_bf16x2(o[k], o[k + 1]);
                         w.y = pack_bf16x2(o[k + 2], o[k + 3]);
                         w.z = pack_bf16x2(o[k + 4], o[k + 5]);
                         w.w = pack_bf16x2(o[k + 6], o[k + 7]);
-                        *reinterpret_cast<uint4*>(orow + q2 * 32 + k) = w;
+                        *reinterpret_cast<uint4*>(orow + q2 * 64 + k) = w;
                     }
                 }
             }
-            // O of this item and the coefficients are read: the issuers may start the next
-            // item's P.V products, the softmax warps may write the next coefficients.
+            // O of this item and the coefficients are read: the P.V issuer may start the
+            // next item's products, the softmax warps may write the next coefficients.
             tc_fence_before();
             __syncwarp();
-            mbar_arrive_if(lane == 0, &bars[BO_FREE + 0]);
-            if (n1 > 0) mbar_arrive_if(lane == 0, &bars[BO_FREE + 1]);
+            mbar_arrive_if(lane == 0, &bars[BO_FREE]);
             mbar_arrive_if(lane == 0, &bars[BCOEF_FREE]);
             ++e;
         }
@@ -698,7 +700,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         const float sl2 = a.scale_log2;
         Cursor cur;
         ItemParams p;
-        uint32_t par = 0;   // bit s: parity of stream s's tiles over all items
+        int g = 0;          // the CTA's tiles over all items
         int ended = 0;      // items handed over to the epilogue warps
         bool ok = true;
         bool have = next_item<G>(a, sch, cur, false, p);
@@ -711,15 +713,13 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int lim = cascade ? p.c - 1 : (row_valid ? p.c + tok : p.c + p.n - 1);  // last key seen
         const bool p_single = p.p_single;
         const int ntiles = p.ntiles;
-        // Running max (log2 domain) and row sum of each stream: even and odd KV tiles
-        // accumulate into separate O buffers and are merged after the last tile.
-        float m_st[2] = {kNoMax, kNoMax};
-        float l_st[2] = {0.f, 0.f};
-        for (int jt = 0; jt < ntiles; ++jt) {
-            const int sm = jt & 1;
-            const uint32_t us = (par >> sm) & 1;   // parity of this tile's use of the buffers
-            const uint32_t tS = tmem + lane_addr + sm * 128;
-            if (!wait_bar_warp(ctl, BS_FULL + sm, us & 1, lane)) { ok = false; break; }
+        // Running max (log2 domain) and row sum.
+        float m_run = kNoMax;
+        float l_run = 0.f;
+        for (int jt = 0; jt < ntiles; ++jt, ++g) {
+            const int b = g % kSBufs;
+            const uint32_t tS = tmem + lane_addr + b * 128;
+            if (!wait_bar_warp(ctl, BS_FULL + b, (g / kSBufs) & 1, lane)) { ok = false; break; }
             tc_fence_after();
             float x[kKeys];
 #pragma unroll
@@ -732,56 +732,121 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int k = 0; k < kKeys; ++k) x[k] = (kbase + k <= lim) ? x[k] : -INFINITY;
             }
-            // Row max over 4 independent chains of three-input max (one softmax warp per
-            // scheduler has no other warp to hide long dependency chains behind).
-            float m4[4];
+            // Optimistic pass (one bf16 P, after an item's first tile): exponentials
+            // against the running max, with no max pass.  A row sum below 2^8 bounds every
+            // p below 2^8, so the row's max did not grow past the lazy threshold and these
+            // are the P and sum the full pass below would compute.  Otherwise (some row's
+            // max grew, or its sum reached 2^8) the warp loads S_jt again, still intact in
+            // TMEM since nothing was stored over it yet, and takes the full pass.  P is
+            // stored only after the check, all 64 columns at once.
+            bool done = false;
+            if (p_single && jt >= 1) {
+                const float m_used = m_run;
+                uint32_t ph[kKeys / 2];
+                float rs8[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) m4[u] = -INFINITY;
+                for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
 #pragma unroll
-            for (int k = 0; k < kKeys; k += 2)
-                m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], x[k], x[k + 1]);
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            const float m_tile = mx * sl2;   // scale > 0: max commutes with scaling
-            // (sm is warp-uniform: selects, not indexed register arrays)
-            const float m_used = sm ? m_st[1] : m_st[0];
-            const bool grow = m_tile > m_used + kLazyRescale;
-            const float m_cur = grow ? m_tile : m_used;
-            // 1 unless grow; 0 when the stream had no key yet.  A row with no key in
-            // this tile keeps m_cur finite (kNoMax at worst), so its p are exp2(-inf) = 0.
-            const float alpha = fast_exp2(m_used - m_cur);
-            // O_sm is rescaled only when some row of the warp grew its max.  The stream's
-            // previous P.V (tile jt - 2) has completed already: S_jt waited for it before
-            // overwriting the buffer; the wait below only makes that visible here.
-            if (jt >= 2 && __any_sync(0xffffffffu, grow)) {
-                if (!wait_bar_warp(ctl, BPV_DONE + sm, (us - 1) & 1, lane)) {
-                    ok = false;
-                    break;
+                for (int e = 0; e < kKeys / 2; ++e) {
+                    float a0, a1;
+                    ffma2(a0, a1, x[2 * e], x[2 * e + 1], sl2, sl2, -m_used, -m_used);
+                    const float p0 = fast_exp2(a0);
+                    const float p1 = fast_exp2(a1);
+                    const int u = (e & 3) * 2;
+                    ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
+                    ph[e] = pack_bf16x2(p0, p1);
                 }
-                tc_fence_after();
+                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
+                                 ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                done = __all_sync(0xffffffffu, rs < kLazyLimit);
+                if (done) {
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    float o[32];
-                    const uint32_t ta = tmem + lane_addr + kTmemO + sm * 128 + q * 32;
-                    tmem_ld32(ta, o);
+                    for (int q = 0; q < kKeys / 32; ++q)
+                        tmem_st16(tS + q * 16,
+                                  *reinterpret_cast<const uint32_t(*)[16]>(&ph[q * 16]));
+                    l_run += rs;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld32(tS + q * 32, *reinterpret_cast<float(*)[32]>(&x[q * 32]));
                     tmem_wait_ld();
+                    if (kbase + kKeys - 1 > lim) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tmem_st32(ta, o);
+                        for (int k = 0; k < kKeys; ++k)
+                            x[k] = (kbase + k <= lim) ? x[k] : -INFINITY;
+                    }
                 }
             }
-            // P_jt over S_jt in the same buffer (S is already in registers): hi in columns
-            // [0, 64), lo in [64, 128), written 32 keys at a time so that few packed
-            // values are live and the exp chains of a chunk overlap.  hi is p truncated
-            // to bf16, lo the exact remainder p - hi truncated to bf16: hi + lo is within
-            // 2^-14 of p (relative), from byte permutes instead of conversions.
-            float rs8[8];
+            if (!done) {
+                // Full pass.  Row max over 4 independent chains of three-input max (one
+                // softmax warp per scheduler has no other warp to hide long dependency
+                // chains behind).
+                float m4[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
-            if (p_single) {
-                // One bf16 P per weight (round to nearest) in columns [0, 64).
+                for (int u = 0; u < 4; ++u) m4[u] = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < kKeys; k += 2)
+                    m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], x[k], x[k + 1]);
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                const float m_tile = mx * sl2;   // scale > 0: max commutes with scaling
+                const float m_used = m_run;
+                const bool grow = m_tile > m_used + kLazyRescale;
+                const float m_cur = grow ? m_tile : m_used;
+                // 1 unless grow; 0 at the item's first tile.  A row with no key in this tile
+                // keeps m_cur finite (kNoMax at worst), so its p are exp2(-inf) = 0.
+                const float alpha = fast_exp2(m_used - m_cur);
+                // O is rescaled only when some row of the warp grew its max, once the P.V
+                // products issued so far (the last one, of tile g - 1, completes last) are
+                // done.  The item's first P.V overwrites O, so its first tile needs none.
+                if (jt >= 1 && __any_sync(0xffffffffu, grow)) {
+                    const int gp = g - 1;
+                    if (!wait_bar_warp(ctl, BPV_DONE + gp % kSBufs, (gp / kSBufs) & 1, lane)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        float o[32];
+                        const uint32_t ta = tmem + lane_addr + kTmemO + q * 32;
+                        tmem_ld32(ta, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st32(ta, o);
+                    }
+                }
+                // P_jt over S_jt in the same buffer (S is already in registers): hi in columns
+                // [0, 64), lo in [64, 128), written 32 keys at a time so that few packed
+                // values are live and the exp chains of a chunk overlap.  hi is p truncated
+                // to bf16, lo the exact remainder p - hi truncated to bf16: hi + lo is within
+                // 2^-14 of p (relative), from byte permutes instead of conversions.
+                float rs8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+                if (p_single) {
+                    // One bf16 P per weight (round to nearest) in columns [0, 64).
+#pragma unroll
+                    for (int q = 0; q < kKeys / 32; ++q) {
+                        uint32_t ph[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int k = q * 32 + 2 * e;
+                            float a0, a1;
+                            ffma2(a0, a1, x[k], x[k + 1], sl2, sl2, -m_cur, -m_cur);
+                            const float p0 = fast_exp2(a0);
+                            const float p1 = fast_exp2(a1);
+                            const int u = (e & 3) * 2;
+                            // row sums by fma with 1 (exact, one rounding as an add)
+                            ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
+                            ph[e] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(tS + q * 16, ph);
+                    }
+                } else {
 #pragma unroll
                 for (int q = 0; q < kKeys / 32; ++q) {
-                    uint32_t ph[16];
+                    uint32_t phi[16], plo[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int k = q * 32 + 2 * e;
@@ -790,49 +855,26 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const float p0 = fast_exp2(a0);
                         const float p1 = fast_exp2(a1);
                         const int u = (e & 3) * 2;
-                        // row sums by fma with 1 (exact, one rounding as an add)
                         ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
-                        ph[e] = pack_bf16x2(p0, p1);
+                        phi[e] = pack_bf16x2_trunc(p0, p1);
+                        float r0, r1;
+                        ffma2(r0, r1, __uint_as_float(__float_as_uint(p0) & 0xffff0000u),
+                              __uint_as_float(__float_as_uint(p1) & 0xffff0000u), -1.f, -1.f, p0, p1);
+                        plo[e] = pack_bf16x2_trunc(r0, r1);
                     }
-                    tmem_st16(tS + q * 16, ph);
+                    tmem_st16(tS + q * 16, phi);
+                    tmem_st16(tS + 64 + q * 16, plo);
                 }
-            } else {
-#pragma unroll
-            for (int q = 0; q < kKeys / 32; ++q) {
-                uint32_t phi[16], plo[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int k = q * 32 + 2 * e;
-                    float a0, a1;
-                    ffma2(a0, a1, x[k], x[k + 1], sl2, sl2, -m_cur, -m_cur);
-                    const float p0 = fast_exp2(a0);
-                    const float p1 = fast_exp2(a1);
-                    const int u = (e & 3) * 2;
-                    ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
-                    phi[e] = pack_bf16x2_trunc(p0, p1);
-                    float r0, r1;
-                    ffma2(r0, r1, __uint_as_float(__float_as_uint(p0) & 0xffff0000u),
-                          __uint_as_float(__float_as_uint(p1) & 0xffff0000u), -1.f, -1.f, p0, p1);
-                    plo[e] = pack_bf16x2_trunc(r0, r1);
                 }
-                tmem_st16(tS + q * 16, phi);
-                tmem_st16(tS + 64 + q * 16, plo);
-            }
-            }
-            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
-                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-            if (sm) {
-                l_st[1] = l_st[1] * alpha + rs;
-                m_st[1] = m_cur;
-            } else {
-                l_st[0] = l_st[0] * alpha + rs;
-                m_st[0] = m_cur;
+                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
+                                 ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                l_run = l_run * alpha + rs;
+                m_run = m_cur;
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            mbar_arrive_if(lane == 0, &bars[BP_FULL + sm]);
-            par ^= 1u << sm;
+            mbar_arrive_if(lane == 0, &bars[BP_FULL + b]);
         }
         if (!ok) break;
         // The next item's parameters, looked up now so that their loads overlap the
@@ -840,26 +882,18 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         ItemParams pn;
         const bool have_next = next_item<G>(a, sch, cur, false, pn);
         // ------------------------------------------------------------ hand-over
-        // Merge the streams: with a_s = 2^(m_s - m), m = max(m_0, m_1),
-        //   O = c_0 O_0 + c_1 O_1,  c_s = a_s / (a_0 l_0 + a_1 l_1).
-        // Stream 0 always holds key 0, which every row sees, so m_0 and l_0 are proper.
-        // The epilogue warps apply it once both streams' last P.V products are done; the
-        // softmax warps go on with the next item.  The coefficients of the previous item
-        // must have been read first (BCOEF_FREE).
+        // The epilogue warps scale O by 1 / l once the item's last P.V product is done;
+        // the softmax warps go on with the next item.  The coefficients of the previous
+        // item must have been read first (BCOEF_FREE).  Every row sees the item's first
+        // key, so l > 0.
         {
-            const int n1 = ntiles >> 1;
             if (ended >= 1 && !wait_bar_warp(ctl, BCOEF_FREE, (ended - 1) & 1, lane)) break;
-            const float m = fmaxf(m_st[0], m_st[1]);
-            const float a0 = fast_exp2(m_st[0] - m);
-            const float a1 = n1 > 0 ? fast_exp2(m_st[1] - m) : 0.f;
-            const float lsum = a0 * l_st[0] + a1 * l_st[1];
             float* coef = reinterpret_cast<float*>(smem + GM::kOffCoef);
-            coef[row] = a0 / lsum;
-            coef[kRows + row] = a1 / lsum;
+            coef[row] = 1.f / l_run;
             if (cascade && row_valid) {
                 const size_t prow = orow_idx * a.max_parts_total + prow_slot;
-                a.m_part[prow] = m;   // log2 domain, as the decode partials
-                a.l_part[prow] = lsum;
+                a.m_part[prow] = m_run;   // log2 domain, as the decode partials
+                a.l_part[prow] = l_run;
             }
             __syncwarp();
             mbar_arrive_if(lane == 0, &bars[BEPI]);
