@@ -119,7 +119,8 @@ struct Geom {
     static constexpr int kOffSreq = kOffBar + kNumBars * 8 + 16;
     static constexpr int kOffOff = kOffSreq + kMaxSchedReqs * 2;
     static constexpr int kOffCoef = kOffOff + (kMaxSchedReqs + 1) * 4;
-    static constexpr int kSmemBytes = kOffCoef + kRows * 4 + 1024;  // + align slack
+    // (the row coefficients, then an exchange array of the two softmax halves)
+    static constexpr int kSmemBytes = kOffCoef + 2 * kRows * 4 + 1024;  // + align slack
 };
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
@@ -127,14 +128,15 @@ constexpr int kMmaWarp = 5;                // issues the S products; owns TMEM
 constexpr int kPvWarp = 6;                 // issues the P.V products
 constexpr int kProducerVWarp = 7;          // V copies (warp 4: Q and K copies)
 constexpr int kEpilogueWarp = 8;           // warps 8-11: epilogue
-constexpr int kThreads = 384;
-// Register split (setmaxnreg) of the three warpgroups: softmax, producer + issuers,
-// epilogue.  The sum over the 384 threads (128 x (248 + 104 + 152) = 64512) must not
-// exceed what the launch provides (384 x the kernel's register count); the launcher
+constexpr int kSoftmaxBWarp = 12;          // warps 12-15: softmax, keys 64-127 of a tile
+constexpr int kThreads = 512;
+// Register split (setmaxnreg) of the four warpgroups: two softmax, copies + issuers,
+// epilogue.  The sum over the 512 threads (128 x (2 x 192 + 64 + 64) = 65536) must not
+// exceed what the launch provides (512 x the kernel's register count); the launcher
 // checks it.
-constexpr int kRegsSoftmax = 248;
-constexpr int kRegsIssue = 104;
-constexpr int kRegsEpilogue = 152;
+constexpr int kRegsSoftmax = 192;
+constexpr int kRegsIssue = 64;
+constexpr int kRegsEpilogue = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;                  // S/P buffers; buffer b at TMEM column 128 b
 constexpr uint32_t kTmemO = 384;           // the O accumulator
@@ -160,6 +162,22 @@ PKV_DEVINL void setmaxnreg_issue() {
 }
 PKV_DEVINL void setmaxnreg_epilogue() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsEpilogue));
+}
+
+// Named barrier `id` of the two partner softmax warps (64 threads).
+PKV_DEVINL void pair_sync(uint32_t id) {
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+// The same barrier, returning whether `v` holds for all 64 threads.
+PKV_DEVINL bool pair_all(uint32_t id, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id)
+        : "memory");
+    return r != 0;
 }
 
 struct Ctl {
@@ -379,7 +397,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                 mbar_init(&bars[BV_FULL + st], 1);
                 mbar_init(&bars[BV_EMPTY + st], 1);
                 mbar_init(&bars[BS_FULL + st], 1);
-                mbar_init(&bars[BP_FULL + st], kSoftmaxWarps);
+                mbar_init(&bars[BP_FULL + st], 2 * kSoftmaxWarps);
                 mbar_init(&bars[BPV_DONE + st], 1);
             }
             mbar_init(&bars[BDRAIN + 0], 1);
@@ -613,11 +631,13 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks) {
                     const uint64_t bv = desc_join(lv + ((ks * 2 * GM::kGroupBytes) >> 4), hi_kv);
-                    umma_bf16_ta_if(leader && ks < ksteps, tO, tS + ks * 8, bv, idesc_pv,
+                    // P of keys 16 ks .. 16 ks + 15: columns 64 h + 8 (ks % 4), h = ks / 4
+                    // (the softmax half that wrote it), lo 32 columns further
+                    const uint32_t tp = tS + (ks >> 2) * 64 + (ks & 3) * 8;
+                    umma_bf16_ta_if(leader && ks < ksteps, tO, tp, bv, idesc_pv,
                                     (j > 0) || (ks > 0));
                     if (!p.p_single)
-                        umma_bf16_ta_if(leader && ks < ksteps, tO, tS + 64 + ks * 8, bv,
-                                        idesc_pv, true);
+                        umma_bf16_ta_if(leader && ks < ksteps, tO, tp + 32, bv, idesc_pv, true);
                 }
                 umma_commit_if(leader, &bars[BPV_DONE + b]);
                 umma_commit_if(leader, &bars[BV_EMPTY + b]);
@@ -627,7 +647,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         umma_commit_if(leader, &bars[BDRAIN + 1]);
         mbar_wait_warp(&bars[BDRAIN + 1], 0, a.status);
     }
-    } else if (warp >= kEpilogueWarp) {
+    } else if (warp >= kEpilogueWarp && warp < kSoftmaxBWarp) {
         setmaxnreg_epilogue();
         // ------------------------------------------------------------ epilogue
         // Warp 8 + q reads TMEM lanes 32 q .. 32 q + 31 (its lane quarter).  Per item: once
@@ -657,30 +677,27 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
             uint16_t* orow = static_cast<uint16_t*>(a.out) + orow_idx * D;
             const size_t prow = orow_idx * a.max_parts_total + p.r;   // cascade: slot = split
 #pragma unroll
-            for (int q2 = 0; q2 < D / 64; ++q2) {
-                float o[64];
-                tmem_ld32(tmem + lane_addr + kTmemO + q2 * 64,
-                          *reinterpret_cast<float(*)[32]>(&o[0]));
-                tmem_ld32(tmem + lane_addr + kTmemO + q2 * 64 + 32,
-                          *reinterpret_cast<float(*)[32]>(&o[32]));
+            for (int q2 = 0; q2 < D / 32; ++q2) {
+                float o[32];
+                tmem_ld32(tmem + lane_addr + kTmemO + q2 * 32, o);
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 64; ++k) o[k] *= c;
+                for (int k = 0; k < 32; ++k) o[k] *= c;
                 if (cascade && row_valid) {
-                    float* dst = a.o_part + prow * D + q2 * 64;
+                    float* dst = a.o_part + prow * D + q2 * 32;
 #pragma unroll
-                    for (int k = 0; k < 64; k += 4)
+                    for (int k = 0; k < 32; k += 4)
                         *reinterpret_cast<float4*>(dst + k) =
                             make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
                 } else if (row_valid) {
 #pragma unroll
-                    for (int k = 0; k < 64; k += 8) {
+                    for (int k = 0; k < 32; k += 8) {
                         uint4 w;
                         w.x = pack_bf16x2(o[k], o[k + 1]);
                         w.y = pack_bf16x2(o[k + 2], o[k + 3]);
                         w.z = pack_bf16x2(o[k + 4], o[k + 5]);
                         w.w = pack_bf16x2(o[k + 6], o[k + 7]);
-                        *reinterpret_cast<uint4*>(orow + q2 * 64 + k) = w;
+                        *reinterpret_cast<uint4*>(orow + q2 * 32 + k) = w;
                     }
                 }
             }
@@ -695,8 +712,24 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
     } else {
         setmaxnreg_softmax();
         // ------------------------------------------------------------ softmax
-        const int row = threadIdx.x;              // 0..127 == TMEM lane
-        const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+        // Two warpgroups: warps 0-3 take keys 0-63 of every KV tile, warps 12-15 keys
+        // 64-127.  Warp w and warp 12 + w share TMEM lane quarter w % 4 (rows 32 w ..
+        // 32 w + 31), one thread per row each, and run on the same scheduler, where each
+        // hides the other's latencies.  The partners keep one running max per row and a
+        // row sum each; they meet at named barrier 1 + w % 4 (64 threads) to agree, per
+        // tile, whether the optimistic pass holds for the whole row and whether to go on
+        // at all (every exit is joint, so neither can be left waiting at a barrier), to
+        // exchange their tile maxima on the full pass, and to add their row sums at the
+        // end of an item.  P of keys 64 h .. 64 h + 63 goes to columns 64 h .. (hi: 32
+        // columns, lo: the next 32) of the buffer: each half stores only over the S it has
+        // loaded itself.
+        const int half = warp >= kSoftmaxBWarp ? 1 : 0;
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;           // == TMEM lane
+        const uint32_t bar_id = 1 + wq;           // the partners' named barrier
+        const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t cbase = 64 * half;         // this half's S / P columns
+        float* xch = reinterpret_cast<float*>(smem + GM::kOffCoef) + kRows;   // exchange
         const float sl2 = a.scale_log2;
         Cursor cur;
         ItemParams p;
@@ -713,122 +746,142 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int lim = cascade ? p.c - 1 : (row_valid ? p.c + tok : p.c + p.n - 1);  // last key seen
         const bool p_single = p.p_single;
         const int ntiles = p.ntiles;
-        // Running max (log2 domain) and row sum.
+        // Running max (log2 domain, the same in both halves) and this half's row sum.
         float m_run = kNoMax;
         float l_run = 0.f;
         for (int jt = 0; jt < ntiles; ++jt, ++g) {
             const int b = g % kSBufs;
-            const uint32_t tS = tmem + lane_addr + b * 128;
-            if (!wait_bar_warp(ctl, BS_FULL + b, (g / kSBufs) & 1, lane)) { ok = false; break; }
-            tc_fence_after();
-            float x[kKeys];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                tmem_ld32(tS + q * 32, *reinterpret_cast<float(*)[32]>(&x[q * 32]));
-            tmem_wait_ld();
-
-            const int kbase = (p.j0 + jt) * kKeys;
-            if (kbase + kKeys - 1 > lim) {
-#pragma unroll
-                for (int k = 0; k < kKeys; ++k) x[k] = (kbase + k <= lim) ? x[k] : -INFINITY;
-            }
+            const uint32_t tS = tmem + lane_addr + b * 128 + cbase;
+            const int kbase = (p.j0 + jt) * kKeys + 64 * half;   // this half's first key
+            bool okw = wait_bar_warp(ctl, BS_FULL + b, (g / kSBufs) & 1, lane);
+            float x[64];
             // Optimistic pass (one bf16 P, after an item's first tile): exponentials
-            // against the running max, with no max pass.  A row sum below 2^8 bounds every
-            // p below 2^8, so the row's max did not grow past the lazy threshold and these
-            // are the P and sum the full pass below would compute.  Otherwise (some row's
-            // max grew, or its sum reached 2^8) the warp loads S_jt again, still intact in
-            // TMEM since nothing was stored over it yet, and takes the full pass.  P is
-            // stored only after the check, all 64 columns at once.
-            bool done = false;
-            if (p_single && jt >= 1) {
-                const float m_used = m_run;
-                uint32_t ph[kKeys / 2];
-                float rs8[8];
+            // against the running max, with no max pass.  A half-row sum below 2^8 bounds
+            // each of its p below 2^8; when that holds for both halves of every row the
+            // rows' maxima did not grow past the lazy threshold, and these are the P and
+            // sums the full pass would compute.  Otherwise both halves load S again (still
+            // intact: nothing was stored over it yet) and take the full pass.
+            const bool try_fast = p_single && jt >= 1;
+            bool good = false;
+            uint32_t ph[32];
+            float rs = 0.f;
+            if (okw) {
+                tc_fence_after();
+                tmem_ld32(tS, *reinterpret_cast<float(*)[32]>(&x[0]));
+                tmem_ld32(tS + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+                tmem_wait_ld();
+                if (kbase + 63 > lim) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
-#pragma unroll
-                for (int e = 0; e < kKeys / 2; ++e) {
-                    float a0, a1;
-                    ffma2(a0, a1, x[2 * e], x[2 * e + 1], sl2, sl2, -m_used, -m_used);
-                    const float p0 = fast_exp2(a0);
-                    const float p1 = fast_exp2(a1);
-                    const int u = (e & 3) * 2;
-                    ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
-                    ph[e] = pack_bf16x2(p0, p1);
+                    for (int k = 0; k < 64; ++k) x[k] = (kbase + k <= lim) ? x[k] : -INFINITY;
                 }
-                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
-                                 ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-                done = __all_sync(0xffffffffu, rs < kLazyLimit);
-                if (done) {
+                if (try_fast) {
+                    float rs8[8];
 #pragma unroll
-                    for (int q = 0; q < kKeys / 32; ++q)
-                        tmem_st16(tS + q * 16,
-                                  *reinterpret_cast<const uint32_t(*)[16]>(&ph[q * 16]));
-                    l_run += rs;
-                } else {
+                    for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        tmem_ld32(tS + q * 32, *reinterpret_cast<float(*)[32]>(&x[q * 32]));
+                    for (int e = 0; e < 32; ++e) {
+                        float a0, a1;
+                        ffma2(a0, a1, x[2 * e], x[2 * e + 1], sl2, sl2, -m_run, -m_run);
+                        const float p0 = fast_exp2(a0);
+                        const float p1 = fast_exp2(a1);
+                        const int u = (e & 3) * 2;
+                        ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
+                        ph[e] = pack_bf16x2(p0, p1);
+                    }
+                    rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
+                         ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                    good = rs < kLazyLimit;
+                }
+            }
+            if (pair_all(bar_id, okw && good)) {
+                tmem_st32(tS, *reinterpret_cast<const float(*)[32]>(&ph[0]));
+                l_run += rs;
+            } else {
+                // Joint exit when either half failed its wait (or saw another role abort).
+                if (!pair_all(bar_id, okw)) { ok = false; break; }
+                if (try_fast) {
+                    tmem_ld32(tS, *reinterpret_cast<float(*)[32]>(&x[0]));
+                    tmem_ld32(tS + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
                     tmem_wait_ld();
-                    if (kbase + kKeys - 1 > lim) {
+                    if (kbase + 63 > lim) {
 #pragma unroll
-                        for (int k = 0; k < kKeys; ++k)
+                        for (int k = 0; k < 64; ++k)
                             x[k] = (kbase + k <= lim) ? x[k] : -INFINITY;
                     }
                 }
-            }
-            if (!done) {
-                // Full pass.  Row max over 4 independent chains of three-input max (one
-                // softmax warp per scheduler has no other warp to hide long dependency
-                // chains behind).
+                // Full pass.  This half's max over 4 independent chains of three-input
+                // max; the partners exchange theirs through shared memory (half 0 writes,
+                // half 1 takes the maximum of both and writes it back).
                 float m4[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) m4[u] = -INFINITY;
 #pragma unroll
-                for (int k = 0; k < kKeys; k += 2)
+                for (int k = 0; k < 64; k += 2)
                     m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], x[k], x[k + 1]);
-                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                if (half == 0) xch[row] = mx;
+                pair_sync(bar_id);
+                if (half == 1) {
+                    mx = fmaxf(mx, xch[row]);
+                    xch[row] = mx;
+                }
+                pair_sync(bar_id);
+                if (half == 0) mx = xch[row];
                 const float m_tile = mx * sl2;   // scale > 0: max commutes with scaling
                 const float m_used = m_run;
                 const bool grow = m_tile > m_used + kLazyRescale;
                 const float m_cur = grow ? m_tile : m_used;
-                // 1 unless grow; 0 at the item's first tile.  A row with no key in this tile
-                // keeps m_cur finite (kNoMax at worst), so its p are exp2(-inf) = 0.
+                // 1 unless grow; 0 at the item's first tile.  A row with no key in this
+                // tile keeps m_cur finite (kNoMax at worst), so its p are exp2(-inf) = 0.
                 const float alpha = fast_exp2(m_used - m_cur);
-                // O is rescaled only when some row of the warp grew its max, once the P.V
-                // products issued so far (the last one, of tile g - 1, completes last) are
-                // done.  The item's first P.V overwrites O, so its first tile needs none.
+                // O is rescaled only when some row of the warp grew its max (the partner
+                // warp has the same rows, so it decides alike), once the P.V products
+                // issued so far (the last one, of tile g - 1, completes last) are done;
+                // each half rescales half of O's columns.  The item's first P.V overwrites
+                // O, so its first tile needs none.  A failed wait is carried to the next
+                // joint decision.
                 if (jt >= 1 && __any_sync(0xffffffffu, grow)) {
                     const int gp = g - 1;
-                    if (!wait_bar_warp(ctl, BPV_DONE + gp % kSBufs, (gp / kSBufs) & 1, lane)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                    okw = wait_bar_warp(ctl, BPV_DONE + gp % kSBufs, (gp / kSBufs) & 1, lane);
+                    if (okw) {
+                        tc_fence_after();
 #pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
-                        float o[32];
-                        const uint32_t ta = tmem + lane_addr + kTmemO + q * 32;
-                        tmem_ld32(ta, o);
-                        tmem_wait_ld();
+                        for (int q = 0; q < D / 64; ++q) {
+                            float o[32];
+                            const uint32_t ta =
+                                tmem + lane_addr + kTmemO + half * (D / 2) + q * 32;
+                            tmem_ld32(ta, o);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tmem_st32(ta, o);
+                            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                            tmem_st32(ta, o);
+                        }
                     }
                 }
-                // P_jt over S_jt in the same buffer (S is already in registers): hi in columns
-                // [0, 64), lo in [64, 128), written 32 keys at a time so that few packed
-                // values are live and the exp chains of a chunk overlap.  hi is p truncated
-                // to bf16, lo the exact remainder p - hi truncated to bf16: hi + lo is within
-                // 2^-14 of p (relative), from byte permutes instead of conversions.
                 float rs8[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
                 if (p_single) {
-                    // One bf16 P per weight (round to nearest) in columns [0, 64).
+                    // One bf16 P per weight (round to nearest) in 32 columns.
 #pragma unroll
-                    for (int q = 0; q < kKeys / 32; ++q) {
-                        uint32_t ph[16];
+                    for (int e = 0; e < 32; ++e) {
+                        float a0, a1;
+                        ffma2(a0, a1, x[2 * e], x[2 * e + 1], sl2, sl2, -m_cur, -m_cur);
+                        const float p0 = fast_exp2(a0);
+                        const float p1 = fast_exp2(a1);
+                        const int u = (e & 3) * 2;
+                        // row sums by fma with 1 (exact, one rounding as an add)
+                        ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
+                        ph[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(tS, *reinterpret_cast<const float(*)[32]>(&ph[0]));
+                } else {
+                    // hi (p truncated to bf16) in 32 columns, lo (the exact remainder
+                    // p - hi, truncated) in the next 32: hi + lo is within 2^-14 of p
+                    // (relative), from byte permutes instead of conversions.
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t phi[16], plo[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int k = q * 32 + 2 * e;
@@ -837,38 +890,21 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const float p0 = fast_exp2(a0);
                             const float p1 = fast_exp2(a1);
                             const int u = (e & 3) * 2;
-                            // row sums by fma with 1 (exact, one rounding as an add)
                             ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
-                            ph[e] = pack_bf16x2(p0, p1);
+                            phi[e] = pack_bf16x2_trunc(p0, p1);
+                            float r0, r1;
+                            ffma2(r0, r1, __uint_as_float(__float_as_uint(p0) & 0xffff0000u),
+                                  __uint_as_float(__float_as_uint(p1) & 0xffff0000u), -1.f,
+                                  -1.f, p0, p1);
+                            plo[e] = pack_bf16x2_trunc(r0, r1);
                         }
-                        tmem_st16(tS + q * 16, ph);
+                        tmem_st16(tS + q * 16, phi);
+                        tmem_st16(tS + 32 + q * 16, plo);
                     }
-                } else {
-#pragma unroll
-                for (int q = 0; q < kKeys / 32; ++q) {
-                    uint32_t phi[16], plo[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int k = q * 32 + 2 * e;
-                        float a0, a1;
-                        ffma2(a0, a1, x[k], x[k + 1], sl2, sl2, -m_cur, -m_cur);
-                        const float p0 = fast_exp2(a0);
-                        const float p1 = fast_exp2(a1);
-                        const int u = (e & 3) * 2;
-                        ffma2(rs8[u], rs8[u + 1], p0, p1, 1.f, 1.f, rs8[u], rs8[u + 1]);
-                        phi[e] = pack_bf16x2_trunc(p0, p1);
-                        float r0, r1;
-                        ffma2(r0, r1, __uint_as_float(__float_as_uint(p0) & 0xffff0000u),
-                              __uint_as_float(__float_as_uint(p1) & 0xffff0000u), -1.f, -1.f, p0, p1);
-                        plo[e] = pack_bf16x2_trunc(r0, r1);
-                    }
-                    tmem_st16(tS + q * 16, phi);
-                    tmem_st16(tS + 64 + q * 16, plo);
                 }
-                }
-                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
-                                 ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-                l_run = l_run * alpha + rs;
+                const float rsf = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
+                                  ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                l_run = l_run * alpha + rsf;
                 m_run = m_cur;
             }
             tmem_wait_st();
@@ -882,21 +918,32 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
         ItemParams pn;
         const bool have_next = next_item<G>(a, sch, cur, false, pn);
         // ------------------------------------------------------------ hand-over
-        // The epilogue warps scale O by 1 / l once the item's last P.V product is done;
-        // the softmax warps go on with the next item.  The coefficients of the previous
-        // item must have been read first (BCOEF_FREE).  Every row sees the item's first
-        // key, so l > 0.
+        // Half 1 passes its row sums to half 0 (the exchange array is free once both
+        // passed the first barrier).  Half 0 writes 1 / l for the epilogue warps, which
+        // scale O once the item's last P.V product is done, while the softmax warps go on
+        // with the next item; the coefficients of the previous item must have been read
+        // first (BCOEF_FREE).  Every row sees the item's first key, so l > 0.
         {
-            if (ended >= 1 && !wait_bar_warp(ctl, BCOEF_FREE, (ended - 1) & 1, lane)) break;
-            float* coef = reinterpret_cast<float*>(smem + GM::kOffCoef);
-            coef[row] = 1.f / l_run;
-            if (cascade && row_valid) {
-                const size_t prow = orow_idx * a.max_parts_total + prow_slot;
-                a.m_part[prow] = m_run;   // log2 domain, as the decode partials
-                a.l_part[prow] = l_run;
+            pair_sync(bar_id);
+            if (half == 1) xch[row] = l_run;
+            pair_sync(bar_id);
+            bool oke = true;
+            if (half == 0) {
+                const float l = l_run + xch[row];
+                oke = ended == 0 || wait_bar_warp(ctl, BCOEF_FREE, (ended - 1) & 1, lane);
+                if (oke) {
+                    float* coef = reinterpret_cast<float*>(smem + GM::kOffCoef);
+                    coef[row] = 1.f / l;
+                    if (cascade && row_valid) {
+                        const size_t prow = orow_idx * a.max_parts_total + prow_slot;
+                        a.m_part[prow] = m_run;   // log2 domain, as the decode partials
+                        a.l_part[prow] = l;
+                    }
+                    __syncwarp();
+                    mbar_arrive_if(lane == 0, &bars[BEPI]);
+                }
             }
-            __syncwarp();
-            mbar_arrive_if(lane == 0, &bars[BEPI]);
+            if (!pair_all(bar_id, oke)) break;
             ++ended;
         }
         p = pn;
@@ -947,7 +994,7 @@ bool register_split_fits(K kern) {
         cudaFuncAttributes attr{};
         if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void*>(kern)) != cudaSuccess)
             return false;
-        const int need = 128 * (kRegsSoftmax + kRegsIssue + kRegsEpilogue);
+        const int need = 128 * (2 * kRegsSoftmax + kRegsIssue + kRegsEpilogue);
         v = attr.numRegs * kThreads >= need ? 1 : 2;
         ok_cached[dev].store(v, std::memory_order_relaxed);
     }
