@@ -131,6 +131,27 @@ PKV_DEVINL void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, u
         : "memory");
 }
 
+// L2 eviction priority of a copy (createpolicy): lines fetched under an evict-first
+// policy are the first ones L2 gives up.  The decode kernels stream every K/V byte
+// exactly once, so they copy under it and leave L2 to what is re-read (query rows,
+// block tables, partials, a shared prefix): on the Llama-3-8B-shaped decode batch this
+// took the step from 90.5 to 86.4 us.
+PKV_DEVINL uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// bulk_g2s under an L2 cache policy.
+PKV_DEVINL void bulk_g2s_hint(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar,
+                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared through a tensor map (coordinates in
 // elements, innermost first).
 PKV_DEVINL void tma_load_3d(void* smem_dst, const void* tmap, int32_t x, int32_t y, int32_t z,
@@ -160,6 +181,30 @@ PKV_DEVINL void tma_load_4d_if(bool on, void* smem_dst, const void* tmap, int32_
         " [%0], [%1, {%2, %3, %4, %5}], [%6];\n\t}" ::"r"(smem_u32(smem_dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
         "r"(static_cast<uint32_t>(on))
+        : "memory");
+}
+
+// tma_load_2d_if / tma_load_4d_if under an L2 cache policy.
+PKV_DEVINL void tma_load_2d_hint_if(bool on, void* smem_dst, const void* tmap, int32_t x,
+                                    int32_t y, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %6;\n\t}" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "r"(static_cast<uint32_t>(on)),
+        "l"(policy)
+        : "memory");
+}
+
+PKV_DEVINL void tma_load_4d_hint_if(bool on, void* smem_dst, const void* tmap, int32_t x,
+                                    int32_t y, int32_t z, int32_t w, uint64_t* bar,
+                                    uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %7, 0;\n\t"
+        "@q cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %8;\n\t}" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
+        "r"(static_cast<uint32_t>(on)), "l"(policy)
         : "memory");
 }
 

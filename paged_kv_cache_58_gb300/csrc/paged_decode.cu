@@ -228,6 +228,7 @@ decode_split_kernel(const DecodeArgs a) {
     };
     fetch_ids(0);
 
+    const uint64_t stream_policy = l2_policy_evict_first();   // K/V are read once
     auto issue = [&](int i, int phys) {  // lane 0 only
         uint8_t* st = ring + (i % kStages) * SM::kStageBytes;
         uint64_t* bar = &bars[i % kStages];
@@ -243,8 +244,8 @@ decode_split_kernel(const DecodeArgs a) {
         const bool stall = a.test_stall && i == 0 && warp == 0 && blockIdx.x == 0 &&
                            blockIdx.y == 0 && blockIdx.z == 0;
         mbar_arrive_expect_tx(bar, SM::kStageBytes + (stall ? 16u : 0u));
-        bulk_g2s(st, kpool + off, SM::kSlab, bar);
-        bulk_g2s(st + SM::kSlab, vpool + off, SM::kSlab, bar);
+        bulk_g2s_hint(st, kpool + off, SM::kSlab, bar, stream_policy);
+        bulk_g2s_hint(st + SM::kSlab, vpool + off, SM::kSlab, bar, stream_policy);
     };
 
     // Prologue: fill the ring.

@@ -19,7 +19,8 @@
 // bf16 hi + lo parts so the probabilities keep ~2^-17 relative precision.
 //
 // Staging: the kernel walks 16-token chunks (a 16-token block, or half of a 32-token
-// one); each chunk's K slab and V slab arrive as one TMA box each, with the 128-byte
+// one); each chunk's K slab and V slab arrive as one TMA box each (under an L2
+// evict-first policy, since no other CTA reads them), with the 128-byte
 // swizzle so that ldmatrix reads them without bank conflicts: for head_dim 128 a 4-D
 // box (the chunk's 16 rows x 256 B as 2 row groups x 2 column halves x 8 rows x 128 B),
 // for head_dim 64 a 16-row x 64-column box.  The warp stays converged throughout: the
@@ -167,6 +168,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
     __syncwarp();
 
+    const uint64_t stream_policy = l2_policy_evict_first();   // K/V are read once
     int ids = -1;
     auto fetch_ids = [&](int base) {
         const int i = base + lane;
@@ -193,9 +195,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         uint8_t* dst = st + (lane == 1 ? SM::kSlab : 0);
         const void* map = lane == 1 ? static_cast<const void*>(&tm_v) : &tm_k;
         if constexpr (D == 128)
-            tma_load_4d_if(mine, dst, map, 0, 0, 0, row / 8, bar);
+            tma_load_4d_hint_if(mine, dst, map, 0, 0, 0, row / 8, bar, stream_policy);
         else
-            tma_load_2d_if(mine, dst, map, 0, row, bar);
+            tma_load_2d_hint_if(mine, dst, map, 0, row, bar, stream_policy);
     };
 
 #pragma unroll
