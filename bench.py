@@ -912,7 +912,8 @@ def main():
                                                                 pb),
                                   dtype=torch.uint8, device=dev)
             h2d = lay.bytes
-            e2e_api = "pkv_paged_decode_append_host (one H2D copy, fused step, one D2H copy)"
+            e2e_api = ("pkv_paged_decode_append_host (pinned buffers: the kernels read the "
+                       "packed inputs from host memory and write the output there in place)")
 
             def e2e_step():
                 pkv.paged_decode_append_host(case.k_pool, case.v_pool, host_in, out_h,

@@ -173,14 +173,18 @@ size_t pkv_paged_decode_append_host_staging_bytes(const pkv_pool_desc* pool, int
                                                   int num_q_heads, int max_blocks_per_seq,
                                                   int max_context, int partition_blocks);
 
-/* One decode step from host memory, queued on `stream`: a copy of host_in
- * (layout.bytes bytes, packed as pkv_decode_step_layout says) into `staging` on the device,
- * pkv_paged_decode_append on the staged arrays, and a copy of the output
- * ([num_seqs][num_q_heads][head_dim], pool dtype) to host_out.  Host buffers should be
- * pinned (page-locked) for the copies to run asynchronously; host_out is complete once
- * the stream has been synchronised, and host_in must stay unchanged until then.
+/* One decode step from host memory, queued on `stream`: pkv_paged_decode_append over
+ * the inputs packed in host_in (layout.bytes bytes, as pkv_decode_step_layout says),
+ * with the output ([num_seqs][num_q_heads][head_dim], pool dtype) going to host_out.
+ * Page-locked host buffers that CUDA maps into the device address space (cudaHostAlloc,
+ * cudaMallocHost, cudaHostRegister; all of them under unified addressing) are read and
+ * written by the kernels in place, over the host link, with no staging copy; other host
+ * memory is copied into `staging` first and the output copied back.  host_out is
+ * complete once the stream has been synchronised, and host_in must stay unchanged until
+ * then.
  *   staging  device, >= pkv_paged_decode_append_host_staging_bytes(...) bytes, 256-byte
- *            aligned; contents need no initialisation and are clobbered.
+ *            aligned; contents need no initialisation and are clobbered (it holds the
+ *            split-KV partials in either case).
  * Argument errors as pkv_paged_decode_append; PKV_ERR_NOMEM if staging is too small. */
 pkv_status pkv_paged_decode_append_host(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
                                         const void* host_in, void* host_out,

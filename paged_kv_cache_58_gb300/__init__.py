@@ -334,9 +334,10 @@ def decode_host_staging_bytes(k_pool, num_seqs, num_q_heads, max_blocks_per_seq,
 def paged_decode_append_host(k_pool, v_pool, host_in, host_out, scale, *, num_seqs, num_q_heads,
                              max_blocks_per_seq, max_context, staging, partition_blocks=0,
                              stream=None):
-    """One decode step from host memory: host_in (pinned uint8, packed as
-    decode_step_layout) -> device staging -> fused append + decode -> host_out (pinned
-    [S, Hq, D]).  Queued on the stream; host_out is complete after a synchronise."""
+    """One decode step from host memory: host_in (uint8, packed as decode_step_layout)
+    -> fused append + decode -> host_out ([S, Hq, D]).  Pinned buffers are read and
+    written by the kernels in place; pageable ones go through `staging` with one copy
+    each way.  Queued on the stream; host_out is complete after a synchronise."""
     if host_in.is_cuda or host_out.is_cuda:
         raise ValueError("host_in and host_out must be host tensors")
     st = _load().pkv_paged_decode_append_host(

@@ -12,11 +12,12 @@
 // tile staged for it serves all G heads.  Per 128-key KV tile j:
 //   S_j = Q K_j^T  tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) into the TMEM
 //                  S/P buffer g % 3 (g: the tile's index over the CTA's items)
-//   softmax        4 warps, one thread per row: tcgen05.ld S_j, causal mask, exp2,
-//                  row sums in fp32; P_j is split into bf16 hi + lo parts (hi = P
+//   softmax        two threads per row, each on half of the tile's keys (warps w and
+//                  12 + w share TMEM lane quarter w): tcgen05.ld S_j, causal mask,
+//                  exp2, row sums in fp32; P_j is split into bf16 hi + lo parts (hi = P
 //                  truncated, lo = the remainder truncated: hi + lo within 2^-14 of P)
-//                  and stored back over S_j in the same TMEM buffer (hi in its first
-//                  64 columns, lo in the next 64)
+//                  and stored back over S_j in the same TMEM buffer (keys 64h..64h+63
+//                  at columns 64h.., hi in 32 columns and lo in the next 32)
 //   O += P_j V_j   two tcgen05.mma passes (A = P hi, then P lo, from TMEM; B = V_j
 //                  from shared memory) into the item's TMEM accumulator O
 // The split keeps the probabilities near fp32 precision: a single bf16 P is off by up
@@ -61,23 +62,24 @@
 //
 // Measured costs per 128-key tile on GB300 (clock64 traces, isolated probes, and copies
 // of this kernel with parts of the work removed): the 16 N = 128 MMAs of a single-P
-// tile take the tensor pipe 1024 cycles (64 each at full rate), the softmax of 128 rows
-// about 1300 cycles on its four warps, and a warp issuing TMA boxes about 100 cycles per
-// box: with all 16 boxes of a tile from one warp the kernel took 0.372 ms on the 16 x
+// tile take the tensor pipe 1024 cycles (64 each at full rate), the softmax about 1450
+// cycles on its two warpgroups, and a warp issuing TMA boxes about 100 cycles per box:
+// with all 16 boxes of a tile from one warp the kernel took 0.372 ms on the 16 x
 // 512-token batch with no softmax work at all, with K and V from two warps 0.308 ms.
 // Shared memory serves about 160 KB a tile (S reads Q and K, P.V reads V, the copies
 // write K and V) at up to 128 B a cycle.  A warp that issues MMAs gets only the issue
-// slots its scheduler's softmax warp leaves free, which is why the issue loops are short.
+// slots its scheduler's softmax warps leave free, which is why the issue loops are short.
 //
-// Warp roles (384 threads, three warpgroups): warps 0-3 softmax (warp w owns TMEM lanes
-// 32w..32w+31), warp 4 barrier set-up + Q and K copies, warp 5 TMEM owner + S issuer,
-// warp 6 P.V issuer, warp 7 V copies, warps 8-11 epilogue (warp 8 + q reads lanes
-// 32q..32q+31).  At the end of an item the softmax warps hand the rows' 1 / l to the
-// epilogue warps through shared memory and go on with the next item; the epilogue warps
-// wait for the item's last P.V product, read the accumulator out, store the output and
-// release the accumulator.  Registers (setmaxnreg): softmax 248 a thread, copies and
-// issuers 104, epilogue 152.  TMEM columns: S/P buffers at [0, 128), [128, 256) and
-// [256, 384); O at [384, 384 + head_dim).
+// Warp roles (512 threads, four warpgroups): warps 0-3 and 12-15 softmax (warps w and
+// 12 + w own TMEM lanes 32w..32w+31, keys 0-63 and 64-127 of each tile; the partners
+// agree per tile through a 64-thread named barrier), warp 4 barrier set-up + Q and K
+// copies, warp 5 TMEM owner + S issuer, warp 6 P.V issuer, warp 7 V copies, warps 8-11
+// epilogue (warp 8 + q reads lanes 32q..32q+31).  At the end of an item the softmax
+// warps hand the rows' 1 / l to the epilogue warps through shared memory and go on with
+// the next item; the epilogue warps wait for the item's last P.V product, read the
+// accumulator out, store the output and release the accumulator.  Registers
+// (setmaxnreg): softmax 192 a thread, copies and issuers 64, epilogue 64.  TMEM
+// columns: S/P buffers at [0, 128), [128, 256) and [256, 384); O at [384, 384 + D).
 #include <atomic>
 #include <cstdlib>
 

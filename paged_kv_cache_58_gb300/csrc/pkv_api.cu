@@ -341,6 +341,19 @@ namespace {
 
 uint64_t round256(uint64_t x) { return (x + 255) / 256 * 256; }
 
+// The address through which kernels reach host memory `p` in place, or nullptr.
+// Page-locked memory from cudaHostAlloc / cudaMallocHost / cudaHostRegister is mapped
+// into the device address space under unified addressing (on a Grace-Blackwell node
+// the GPU then reads and writes it over NVLink-C2C); pageable memory is not.
+void* mapped_host_ptr(const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();   // a failed query is left as the last error: clear it
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 }  // namespace
 
 pkv_status pkv_decode_step_layout(const pkv_pool_desc* pool, int num_seqs, int num_q_heads,
@@ -402,15 +415,23 @@ pkv_status pkv_paged_decode_append_host(const pkv_pool_desc* pool, void* k_pool,
     char* out = dev + l.bytes;
     char* ws = out + round256(out_bytes);
     const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(dev, host_in, l.bytes, cudaMemcpyHostToDevice, st_) != cudaSuccess)
-        return PKV_ERR_CUDA;
-    st = pkv_paged_decode_append(pool, out, dev + l.q, k_pool, v_pool, dev + l.k_new,
-                                 dev + l.v_new, reinterpret_cast<const int32_t*>(dev + l.block_tables),
+    // Mapped (page-locked) host buffers are read and written by the kernels in place;
+    // any other host memory goes through the staging buffer with one copy each way.
+    const char* in = static_cast<const char*>(mapped_host_ptr(host_in));
+    char* out_map = static_cast<char*>(mapped_host_ptr(host_out));
+    if (!in) {
+        if (cudaMemcpyAsync(dev, host_in, l.bytes, cudaMemcpyHostToDevice, st_) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        in = dev;
+    }
+    st = pkv_paged_decode_append(pool, out_map ? out_map : out, in + l.q, k_pool, v_pool,
+                                 in + l.k_new, in + l.v_new,
+                                 reinterpret_cast<const int32_t*>(in + l.block_tables),
                                  max_blocks_per_seq,
-                                 reinterpret_cast<const int32_t*>(dev + l.context_lens),
+                                 reinterpret_cast<const int32_t*>(in + l.context_lens),
                                  max_context, num_seqs, num_q_heads, scale, partition_blocks, ws,
                                  need - (ws - dev), stream);
-    if (st != PKV_OK) return st;
+    if (st != PKV_OK || out_map) return st;
     return from_cuda(cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, st_));
 }
 

@@ -155,11 +155,13 @@ def test_fused_rejects_bad_new_rows(pkv):
                                 case.scale, max_context=case.max_context)
 
 
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
 @pytest.mark.parametrize("wl_name,lengths", [("8b", None), ("tiny", None),
                                              ("8b", [1, 16, 17, 4000, 33])])
-def test_host_step_matches_device_call(pkv, wl_name, lengths):
-    """pkv_paged_decode_append_host (inputs and output in pinned host memory, one copy
-    each way) gives the device-buffer call's output bits and pools."""
+def test_host_step_matches_device_call(pkv, wl_name, lengths, pinned):
+    """pkv_paged_decode_append_host gives the device-buffer call's output bits and pools,
+    with pinned host buffers (the kernels read the inputs and write the output in place)
+    and with pageable ones (one copy each way through the staging buffer)."""
     kw = {} if lengths is None else {"lengths": lengths, "seed": 41}
     a = synth.build_case(wl_name, "cuda", **kw)
     b = synth.build_case(wl_name, "cuda", **kw)
@@ -167,10 +169,13 @@ def test_host_step_matches_device_call(pkv, wl_name, lengths):
     mbs = a.block_tables.shape[1]
     out_dev = fused(pkv, b)
     lay = pkv.decode_step_layout(a.k_pool, S, Hq, mbs)
-    host_in = torch.empty(lay.bytes, dtype=torch.uint8).pin_memory()
+    host_in = torch.empty(lay.bytes, dtype=torch.uint8)
+    host_out = torch.full((S, Hq, D), float("nan"), dtype=a.q.dtype)
+    if pinned:
+        host_in, host_out = host_in.pin_memory(), host_out.pin_memory()
+    assert host_in.is_pinned() == pinned and host_out.is_pinned() == pinned
     pkv.pack_decode_step(host_in, lay, a.q.cpu(), a.k_new.cpu(), a.v_new.cpu(),
                          a.block_tables.cpu(), a.context_lens.cpu())
-    host_out = torch.empty((S, Hq, D), dtype=a.q.dtype).pin_memory()
     staging = torch.empty(pkv.decode_host_staging_bytes(a.k_pool, S, Hq, mbs, a.max_context),
                           dtype=torch.uint8, device="cuda")
     pkv.paged_decode_append_host(a.k_pool, a.v_pool, host_in, host_out, a.scale, num_seqs=S,
