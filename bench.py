@@ -245,14 +245,15 @@ def append_bytes_of(k_new, slot_mapping):
 
 
 def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf16",
-                  peaks_=None, cpu=True):
+                  peaks_=None, cpu=True, e2e=True):
     """Prefix-cached chunked prefill (16 requests x 512 new tokens over cached
     prefixes of U[1024, 8192]) measured three ways: the kv_append of the 8192 new rows
     alone (L2 flushed before each call: its 67 MB fit in L2), the prefill call alone
     (K/V of 335 MB per call > L2), and the workload's step, append then prefill, K
     times back to back.  block_size, head_dim and dtype vary the recipe (the pool keeps
-    its byte size).  With `cpu` the oracle prefill is timed on the host cores over the
-    first requests of the batch."""
+    its byte size).  With `e2e` the step is also timed end to end from pinned host
+    buffers; with `cpu` the oracle prefill is timed on the host cores over the first
+    requests of the batch."""
     import dataclasses
     import torch
     import synth
@@ -326,11 +327,54 @@ def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf
                                    "peak_kind": f"{kind} hbm_gbs",
                                    "frac_of_8tbs": ab / sustained_s / 1e9 / NOMINAL_HBM_GBS,
                                    "traffic": None}}}
+    if e2e:
+        res["e2e"] = prefill_e2e(pkv, case, out, max_new, steps, stream, flops)
     if cpu:
         res["cpu_baseline"] = prefill_cpu_baseline(case, flops)
     del case, out
     torch.cuda.empty_cache()
     return res
+
+
+def prefill_e2e(pkv, case, out, max_new, steps, stream, flops):
+    """The prefill step end to end from pinned host memory, per step: the step's inputs
+    (q, the new K/V rows and their slots, the block tables, the requests' cached and new
+    lengths and q offsets) copied to the device, kv_append + paged_prefill, the output
+    copied back, and a synchronise.  Host seconds over `steps` steps."""
+    import torch
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "cached_lens",
+             "new_lens", "q_offsets")
+    host = {n: getattr(case, n).cpu().pin_memory() for n in names}
+    devb = {n: torch.empty_like(getattr(case, n)) for n in names}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def step():
+        with torch.cuda.stream(stream):
+            for n in names:
+                devb[n].copy_(host[n], non_blocking=True)
+        pkv.kv_append(case.k_pool, case.v_pool, devb["slot_mapping"], devb["k_new"],
+                      devb["v_new"], stream=stream)
+        pkv.paged_prefill(devb["q"], case.k_pool, case.v_pool, devb["block_tables"],
+                          devb["cached_lens"], devb["new_lens"], devb["q_offsets"],
+                          case.scale, max_new=max_new, out=out, stream=stream)
+        with torch.cuda.stream(stream):
+            out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        step()
+    assert pkv.read_device_status() == 0
+    assert torch.equal(out_h.view(torch.uint8), out.cpu().view(torch.uint8))
+    clock = WallClock()
+    clock.begin()
+    for _ in range(steps):
+        step()
+    sec = clock.end() / steps
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "ms_per_step": sec * 1e3,
+            "api": "torch H2D copies + kv_append + paged_prefill + torch D2H copy",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
+            "steps": steps}
 
 
 def append_sustained(pkv, case, steps, stream, sets=4):
@@ -946,7 +990,7 @@ def main():
     if not args.no_prefill:
         prefill = bench_prefill(pkv, dev, args.prefill_steps, stream, args.block_size,
                                 args.prefill_head_dim, args.prefill_dtype, pk,
-                                cpu=not args.no_cpu_baseline)
+                                cpu=not args.no_cpu_baseline, e2e=not args.no_e2e)
         if prefill["dtype"] == "f32":
             # fp32 pools run on the CUDA cores: fp32 FMA peak from the unit counts and the
             # maximum SM clock (152 SMs x 128 FMA a clock x 2 flop x 2.07 GHz).
