@@ -295,7 +295,7 @@ def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf
     ms = time_calls(call, steps, stream) * 1e3
     flush = L2Flush(dev)
     append_s = time_calls(append, steps, stream, before=flush)
-    sustained_s = append_sustained(pkv, case, steps, stream)
+    sustained_s, eager_s = append_sustained(pkv, case, steps, stream)
     clock = EventClock(stream)
     clock.sync()
     clock.begin()
@@ -319,7 +319,9 @@ def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf
            "append": {"kernel": "kv_append_kernel", "rows": int(case.k_new.shape[0]),
                       "bytes_per_call": ab, "ms": sustained_s * 1e3,
                       "timing": ("calls back to back over 4 rotating sets of new rows and "
-                                 "slots (268 MB, larger than L2), CUDA events around all"),
+                                 "slots (268 MB, larger than L2), replayed from a CUDA graph, "
+                                 "CUDA events around all"),
+                      "ms_eager_back_to_back": eager_s * 1e3,
                       "ms_single_call_l2_flushed": append_s * 1e3,
                       "roofline": {"bound": "hbm", "achieved": ab / sustained_s / 1e9,
                                    "peak": hbm, "unit": "GB/s",
@@ -382,7 +384,8 @@ def append_sustained(pkv, case, steps, stream, sets=4):
     back to back: `sets` different sets of new rows, each with its own slots in pool
     blocks no block table references, used in turn, so that what a call reads and
     writes was last touched sets - 1 calls earlier (268 MB in between at 4 sets, more
-    than L2 holds).  The workload's own pool contents are left as they are."""
+    than L2 holds).  The workload's own pool contents are left as they are.  Returns
+    (seconds per call replayed from a CUDA graph, seconds per call launched eagerly)."""
     import torch
     nb, _, B, _ = case.k_pool.shape
     T = case.k_new.shape[0]
@@ -392,7 +395,7 @@ def append_sustained(pkv, case, steps, stream, sets=4):
     free = torch.nonzero(~used).flatten()
     per = -(-T // B)
     if free.numel() < sets * per:
-        return float("nan")
+        return float("nan"), float("nan")
     g = torch.Generator(device=case.k_pool.device).manual_seed(77)
     data = []
     for i in range(sets):
@@ -407,16 +410,34 @@ def append_sustained(pkv, case, steps, stream, sets=4):
     for i in range(2 * sets):
         sl, kn, vn = data[i % sets]
         pkv.kv_append(case.k_pool, case.v_pool, sl, kn, vn, stream=stream)
+    n = max(steps, 2 * sets)
     clock = EventClock(stream)
     clock.sync()
     clock.begin()
-    n = max(steps, 2 * sets)
     for i in range(n):
         sl, kn, vn = data[i % sets]
         pkv.kv_append(case.k_pool, case.v_pool, sl, kn, vn, stream=stream)
-    sec = clock.end() / n
+    eager = clock.end() / n
+    # The same n calls captured once in a CUDA graph and replayed: back to back on the
+    # GPU without the Python call between launches (a ~10 us kernel is shorter than
+    # the host side of one call).
+    gs = torch.cuda.Stream(device=case.k_pool.device)
+    gs.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for i in range(n):
+            sl, kn, vn = data[i % sets]
+            pkv.kv_append(case.k_pool, case.v_pool, sl, kn, vn, stream=gs)
+    with torch.cuda.stream(gs):   # replay() launches on the current stream
+        graph.replay()
+        gclock = EventClock(gs)
+        gclock.sync()
+        gclock.begin()
+        graph.replay()
+        sec = gclock.end() / n
     assert pkv.read_device_status() == 0
-    return sec
+    del graph
+    return sec, eager
 
 
 def prefill_cpu_baseline(case, flops_all, budget_s=10.0):

@@ -49,6 +49,44 @@ kv_append_kernel(uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
     *reinterpret_cast<uint4*>(v_pool + dst) = vv;
 }
 
+// The same scatter with the index arithmetic cut down: chunks per row (8, 16 or 32 for
+// the supported head dims and dtypes) is a compile-time constant, the block size a power
+// of two, and the chunk index fits 32 bits (the launcher checks), so the decomposition
+// is shifts, masks and one 32-bit division instead of five 64-bit divisions.  At about
+// 10 us for 8192 rows the general kernel's integer divisions were a visible share.
+template <int CPR>
+__global__ void __launch_bounds__(256)
+kv_append_pow2_kernel(uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
+                      const int64_t* __restrict__ slots, const uint8_t* __restrict__ k,
+                      const uint8_t* __restrict__ v, uint32_t num_chunks, uint32_t num_kv_heads,
+                      int block_shift, int64_t num_slots, int* status) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const uint32_t idx = blockIdx.x * 256u + threadIdx.x;
+    if (idx >= num_chunks) return;
+    const uint32_t chunk = idx % CPR;
+    const uint32_t row = idx / CPR;                 // (token, head)
+    const uint32_t tok = row / num_kv_heads;
+    const uint32_t head = row - tok * num_kv_heads;
+    // The row's data do not depend on its slot: their loads go out beside the slot's, so
+    // a thread waits for one memory round trip before its stores, not two.
+    const int64_t src = (static_cast<int64_t>(row) * CPR + chunk) * 16;
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(k + src));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(v + src));
+    const int64_t slot = __ldg(slots + tok);
+    if (slot < 0) return;                           // padding row
+    if (slot >= num_slots) {
+        raise_status(status, PKV_ERR_OOB);
+        return;
+    }
+    const int64_t blk = slot >> block_shift;
+    const int64_t off = slot & ((int64_t{1} << block_shift) - 1);
+    const int64_t dst =
+        ((((blk * num_kv_heads + head) << block_shift) + off) * CPR + chunk) * 16;
+    *reinterpret_cast<uint4*>(k_pool + dst) = kv;
+    *reinterpret_cast<uint4*>(v_pool + dst) = vv;
+}
+
 // grid (pairs, 2): y selects the K or V pool; one CTA copies one whole block.
 __global__ void __launch_bounds__(256)
 copy_blocks_kernel(uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
@@ -79,6 +117,19 @@ cudaError_t launch_kv_append(void* k_pool, void* v_pool, const int64_t* slot_map
     const int64_t num_chunks = num_tokens * num_kv_heads * chunks_per_row;
     if (num_chunks == 0) return cudaSuccess;
     const int64_t grid = (num_chunks + 255) / 256;
+    const int block_shift = block_size == 16 ? 4 : block_size == 32 ? 5 : -1;
+    if (num_chunks < (int64_t{1} << 31) && block_shift > 0 &&
+        (chunks_per_row == 8 || chunks_per_row == 16 || chunks_per_row == 32)) {
+        auto kern = chunks_per_row == 8    ? kv_append_pow2_kernel<8>
+                    : chunks_per_row == 16 ? kv_append_pow2_kernel<16>
+                                           : kv_append_pow2_kernel<32>;
+        return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream,
+                          static_cast<uint8_t*>(k_pool), static_cast<uint8_t*>(v_pool),
+                          slot_mapping, static_cast<const uint8_t*>(k),
+                          static_cast<const uint8_t*>(v), static_cast<uint32_t>(num_chunks),
+                          static_cast<uint32_t>(num_kv_heads), block_shift,
+                          num_blocks * block_size, status);
+    }
     return launch_pdl(kv_append_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream,
                       static_cast<uint8_t*>(k_pool), static_cast<uint8_t*>(v_pool), slot_mapping,
                       static_cast<const uint8_t*>(k), static_cast<const uint8_t*>(v), num_chunks,

@@ -416,9 +416,12 @@ pkv_status pkv_paged_decode_append_host(const pkv_pool_desc* pool, void* k_pool,
     char* ws = out + round256(out_bytes);
     const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
     // Mapped (page-locked) host buffers are read and written by the kernels in place;
-    // any other host memory goes through the staging buffer with one copy each way.
+    // any other host memory, or a buffer not 16-byte aligned (the kernels' vector
+    // accesses need that), goes through the staging buffer with one copy each way.
     const char* in = static_cast<const char*>(mapped_host_ptr(host_in));
     char* out_map = static_cast<char*>(mapped_host_ptr(host_out));
+    if (!aligned16(in)) in = nullptr;
+    if (!aligned16(out_map)) out_map = nullptr;
     if (!in) {
         if (cudaMemcpyAsync(dev, host_in, l.bytes, cudaMemcpyHostToDevice, st_) != cudaSuccess)
             return PKV_ERR_CUDA;

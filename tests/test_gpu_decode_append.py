@@ -155,13 +155,14 @@ def test_fused_rejects_bad_new_rows(pkv):
                                 case.scale, max_context=case.max_context)
 
 
-@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+@pytest.mark.parametrize("pinned", ["pinned", "pageable", "pinned_unaligned"])
 @pytest.mark.parametrize("wl_name,lengths", [("8b", None), ("tiny", None),
                                              ("8b", [1, 16, 17, 4000, 33])])
 def test_host_step_matches_device_call(pkv, wl_name, lengths, pinned):
     """pkv_paged_decode_append_host gives the device-buffer call's output bits and pools,
-    with pinned host buffers (the kernels read the inputs and write the output in place)
-    and with pageable ones (one copy each way through the staging buffer)."""
+    with pinned host buffers (the kernels read the inputs and write the output in place),
+    with pageable ones and with pinned ones off a 16-byte boundary (one copy each way
+    through the staging buffer)."""
     kw = {} if lengths is None else {"lengths": lengths, "seed": 41}
     a = synth.build_case(wl_name, "cuda", **kw)
     b = synth.build_case(wl_name, "cuda", **kw)
@@ -169,11 +170,21 @@ def test_host_step_matches_device_call(pkv, wl_name, lengths, pinned):
     mbs = a.block_tables.shape[1]
     out_dev = fused(pkv, b)
     lay = pkv.decode_step_layout(a.k_pool, S, Hq, mbs)
-    host_in = torch.empty(lay.bytes, dtype=torch.uint8)
-    host_out = torch.full((S, Hq, D), float("nan"), dtype=a.q.dtype)
-    if pinned:
-        host_in, host_out = host_in.pin_memory(), host_out.pin_memory()
-    assert host_in.is_pinned() == pinned and host_out.is_pinned() == pinned
+    esz = a.q.element_size()
+    if pinned == "pinned_unaligned":
+        # views 8 bytes (input) and one element (output) past 16-byte aligned storage
+        host_in = torch.empty(lay.bytes + 16, dtype=torch.uint8).pin_memory()[8:8 + lay.bytes]
+        raw = torch.empty((S * Hq * D + 16) * esz, dtype=torch.uint8).pin_memory()
+        host_out = raw[esz:esz + S * Hq * D * esz].view(a.q.dtype).view(S, Hq, D)
+        host_out.fill_(float("nan"))
+        assert host_in.data_ptr() % 16 == 8 and host_out.data_ptr() % 16 != 0
+    else:
+        host_in = torch.empty(lay.bytes, dtype=torch.uint8)
+        host_out = torch.full((S, Hq, D), float("nan"), dtype=a.q.dtype)
+        if pinned == "pinned":
+            host_in, host_out = host_in.pin_memory(), host_out.pin_memory()
+    assert host_in.is_pinned() == (pinned != "pageable")
+    assert host_out.is_pinned() == (pinned != "pageable")
     pkv.pack_decode_step(host_in, lay, a.q.cpu(), a.k_new.cpu(), a.v_new.cpu(),
                          a.block_tables.cpu(), a.context_lens.cpu())
     staging = torch.empty(pkv.decode_host_staging_bytes(a.k_pool, S, Hq, mbs, a.max_context),
