@@ -12,6 +12,8 @@
 // 128-bit and fully coalesced within a row.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -118,7 +120,11 @@ cudaError_t launch_kv_append(void* k_pool, void* v_pool, const int64_t* slot_map
     if (num_chunks == 0) return cudaSuccess;
     const int64_t grid = (num_chunks + 255) / 256;
     const int block_shift = block_size == 16 ? 4 : block_size == 32 ? 5 : -1;
-    if (num_chunks < (int64_t{1} << 31) && block_shift > 0 &&
+    // PKV_TEST_APPEND_GENERIC=1 sends every append to the general kernel (read at each
+    // call; tests only: otherwise it runs for 2^31 chunks or more).
+    const char* force = std::getenv("PKV_TEST_APPEND_GENERIC");
+    const bool generic = force != nullptr && force[0] == '1';
+    if (!generic && num_chunks < (int64_t{1} << 31) && block_shift > 0 &&
         (chunks_per_row == 8 || chunks_per_row == 16 || chunks_per_row == 32)) {
         auto kern = chunks_per_row == 8    ? kv_append_pow2_kernel<8>
                     : chunks_per_row == 16 ? kv_append_pow2_kernel<16>

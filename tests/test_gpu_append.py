@@ -19,9 +19,15 @@ def pkv():
     return m
 
 
+@pytest.mark.parametrize("kernel", ["pow2", "generic"])
 @pytest.mark.parametrize("dtype,d,hkv", [(torch.bfloat16, 128, 8), (torch.bfloat16, 64, 2),
-                                         (torch.float32, 128, 4), (torch.float32, 64, 1)])
-def test_kv_append_bit_exact(pkv, oracle_mod, dtype, d, hkv):
+                                         (torch.float32, 128, 4), (torch.float32, 64, 1),
+                                         (torch.bfloat16, 128, 3)])
+def test_kv_append_bit_exact(pkv, oracle_mod, dtype, d, hkv, kernel, monkeypatch):
+    """Both append kernels (the general one normally runs only past 2^31 chunks; the
+    test hook sends these calls to it) against the oracle scatter, bit for bit."""
+    if kernel == "generic":
+        monkeypatch.setenv("PKV_TEST_APPEND_GENERIC", "1")
     g = torch.Generator().manual_seed(d + hkv)
     nb, T = 40, 300
     kp = torch.randn((nb, hkv, 16, d), generator=g).to(dtype).cuda()
