@@ -977,15 +977,18 @@ def main():
                                                                 pb),
                                   dtype=torch.uint8, device=dev)
             h2d = lay.bytes
-            e2e_api = ("pkv_paged_decode_append_host (pinned buffers: the kernels read the "
-                       "packed inputs from host memory and write the output there in place)")
+            e2e_api = ("pkv_paged_decode_append_host through HostDecodeStep (pinned buffers: "
+                       "the kernels read the packed inputs from host memory and write the "
+                       "output there in place)")
+
+            host_step = pkv.HostDecodeStep(case.k_pool, case.v_pool, host_in, out_h,
+                                           case.scale, num_seqs=S, num_q_heads=Hq,
+                                           max_blocks_per_seq=mbs, max_context=max_ctx,
+                                           staging=staging, partition_blocks=pb,
+                                           stream=stream)
 
             def e2e_step():
-                pkv.paged_decode_append_host(case.k_pool, case.v_pool, host_in, out_h,
-                                             case.scale, num_seqs=S, num_q_heads=Hq,
-                                             max_blocks_per_seq=mbs, max_context=max_ctx,
-                                             staging=staging, partition_blocks=pb,
-                                             stream=stream)
+                host_step()
                 stream.synchronize()
 
         for _ in range(max(3, args.warmup)):

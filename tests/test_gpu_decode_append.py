@@ -197,3 +197,36 @@ def test_host_step_matches_device_call(pkv, wl_name, lengths, pinned):
     assert torch.equal(host_out.view(torch.uint8), out_dev.cpu().view(torch.uint8))
     assert torch.equal(a.k_pool.view(torch.uint8), b.k_pool.view(torch.uint8))
     assert torch.equal(a.v_pool.view(torch.uint8), b.v_pool.view(torch.uint8))
+
+
+def test_host_decode_step_plan_repeats_the_call(pkv):
+    """HostDecodeStep (arguments bound once) gives the keyword call's output bits on
+    every call, with the host buffer refilled in between."""
+    a = synth.build_case("8b", "cuda")
+    S, Hq, D = a.q.shape
+    mbs = a.block_tables.shape[1]
+    lay = pkv.decode_step_layout(a.k_pool, S, Hq, mbs)
+    host_in = torch.empty(lay.bytes, dtype=torch.uint8).pin_memory()
+    pkv.pack_decode_step(host_in, lay, a.q.cpu(), a.k_new.cpu(), a.v_new.cpu(),
+                         a.block_tables.cpu(), a.context_lens.cpu())
+    staging = torch.empty(pkv.decode_host_staging_bytes(a.k_pool, S, Hq, mbs, a.max_context),
+                          dtype=torch.uint8, device="cuda")
+    ref = torch.empty((S, Hq, D), dtype=a.q.dtype).pin_memory()
+    kw = dict(num_seqs=S, num_q_heads=Hq, max_blocks_per_seq=mbs, max_context=a.max_context,
+              staging=staging)
+    pkv.paged_decode_append_host(a.k_pool, a.v_pool, host_in, ref, a.scale, **kw)
+    torch.cuda.synchronize()
+    out = torch.full((S, Hq, D), float("nan"), dtype=a.q.dtype).pin_memory()
+    step = pkv.HostDecodeStep(a.k_pool, a.v_pool, host_in, out, a.scale, **kw)
+    for i in range(3):
+        out.fill_(float("nan"))
+        q2 = a.q.cpu() * (1 + i)   # a different query each call, same new rows
+        pkv.pack_decode_step(host_in, lay, q2, a.k_new.cpu(), a.v_new.cpu(),
+                             a.block_tables.cpu(), a.context_lens.cpu())
+        step()
+        torch.cuda.synchronize()
+        pkv.paged_decode_append_host(a.k_pool, a.v_pool, host_in, ref, a.scale, **kw)
+        torch.cuda.synchronize()
+        assert pkv.read_device_status() == 0
+        assert torch.equal(out.view(torch.uint8), ref.view(torch.uint8))
+
