@@ -9,6 +9,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/pkv.h"
 #include "kernels.h"
 #include "prefill_f32.h"
@@ -63,6 +65,17 @@ cudaStream_t side_stream() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// An NVTX range around each call that enqueues GPU work, named after the call, so that
+// a profiler's timeline groups the call's kernels under it and ncu can select them
+// (--nvtx --nvtx-include "pkv_paged_decode/").  With no tool attached a push and a pop
+// cost a few nanoseconds.
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange&) = delete;
+    CallRange& operator=(const CallRange&) = delete;
+};
 
 int elem_bytes(int dtype) { return dtype == PKV_BF16 ? 2 : 4; }
 
@@ -206,6 +219,7 @@ uint64_t pkv_pool_bytes(const pkv_pool_desc* pool) {
 pkv_status pkv_kv_append(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
                          const int64_t* slot_mapping, const void* k, const void* v,
                          int64_t num_tokens, void* stream) {
+    CallRange range("pkv_kv_append");
     pkv_status st = check_pool(pool);
     if (st != PKV_OK) return st;
     if (num_tokens < 0) return PKV_ERR_INVALID;
@@ -318,6 +332,7 @@ pkv_status pkv_paged_decode(const pkv_pool_desc* pool, void* out, const void* q,
                             const int32_t* context_lens, int max_context, int num_seqs,
                             int num_q_heads, float scale, int partition_blocks,
                             void* workspace, size_t workspace_bytes, void* stream) {
+    CallRange range("pkv_paged_decode");
     return decode_impl(pool, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
                        context_lens, max_context, num_seqs, num_q_heads, scale,
                        partition_blocks, workspace, workspace_bytes, nullptr, nullptr, stream);
@@ -330,6 +345,7 @@ pkv_status pkv_paged_decode_append(const pkv_pool_desc* pool, void* out, const v
                                    int max_context, int num_seqs, int num_q_heads, float scale,
                                    int partition_blocks, void* workspace, size_t workspace_bytes,
                                    void* stream) {
+    CallRange range("pkv_paged_decode_append");
     if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
         return PKV_ERR_INVALID;
     return decode_impl(pool, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
@@ -398,6 +414,7 @@ pkv_status pkv_paged_decode_append_host(const pkv_pool_desc* pool, void* k_pool,
                                         int max_blocks_per_seq, int max_context, int num_seqs,
                                         int num_q_heads, float scale, int partition_blocks,
                                         void* staging, size_t staging_bytes, void* stream) {
+    CallRange range("pkv_paged_decode_append_host");
     pkv_step_layout l;
     pkv_status st = pkv_decode_step_layout(pool, num_seqs, num_q_heads, max_blocks_per_seq, &l);
     if (st != PKV_OK) return st;
@@ -444,6 +461,7 @@ pkv_status pkv_paged_decode_noalloc(const pkv_pool_desc* pool, void* out, const 
                                     const int32_t* context_lens, int max_context, int num_seqs,
                                     int num_q_heads, float scale, int partition_blocks,
                                     void* stream) {
+    CallRange range("pkv_paged_decode_noalloc");
     pkv_status st = check_pool(pool);
     if (st != PKV_OK) return st;
     if (num_seqs < 0 || num_q_heads <= 0 || partition_blocks < 0 || max_context <= 0)
@@ -665,6 +683,7 @@ pkv_status pkv_paged_decode_cascade(const pkv_pool_desc* pool, void* out, const 
                                     const int32_t* context_lens, int max_context, int num_seqs,
                                     int num_q_heads, float scale, int partition_blocks,
                                     void* workspace, size_t workspace_bytes, void* stream) {
+    CallRange range("pkv_paged_decode_cascade");
     return cascade_impl(pool, out, q, k_pool, v_pool, prefix_blocks, prefix_len, block_tables,
                         max_blocks_per_seq, context_lens, max_context, num_seqs, num_q_heads,
                         scale, partition_blocks, workspace, workspace_bytes, nullptr, nullptr,
@@ -679,6 +698,7 @@ pkv_status pkv_paged_decode_cascade_append(const pkv_pool_desc* pool, void* out,
                                            int max_context, int num_seqs, int num_q_heads,
                                            float scale, int partition_blocks, void* workspace,
                                            size_t workspace_bytes, void* stream) {
+    CallRange range("pkv_paged_decode_cascade_append");
     if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
         return PKV_ERR_INVALID;
     return cascade_impl(pool, out, q, k_pool, v_pool, prefix_blocks, prefix_len, block_tables,
@@ -693,6 +713,7 @@ pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q
                              const int32_t* cached_lens, const int32_t* new_lens,
                              const int32_t* q_offsets, int num_reqs, int total_new, int max_new,
                              int num_q_heads, float scale, void* stream) {
+    CallRange range("pkv_paged_prefill");
     pkv_status st = check_pool(pool);
     if (st != PKV_OK) return st;
     if (num_reqs < 0 || total_new < 0 || max_new < 0 || num_q_heads <= 0 || !(scale > 0.f))
@@ -741,6 +762,7 @@ pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q
 
 pkv_status pkv_copy_blocks(const pkv_pool_desc* pool, void* k_pool, void* v_pool,
                            const int32_t* pairs, int num_pairs, void* stream) {
+    CallRange range("pkv_copy_blocks");
     pkv_status st = check_pool(pool);
     if (st != PKV_OK) return st;
     if (num_pairs < 0) return PKV_ERR_INVALID;
