@@ -7,19 +7,22 @@
 // That Does Not Forget"), for fp32 K/V, where the tensor cores would round the
 // operands to tf32.  FlashAttention-style tiling on the FMA pipe:
 //
-// One CTA (256 threads) computes one 64-row query tile: 64 / G consecutive new tokens
-// x the G query heads of kv head `kvh` (rows token-major, heads inner), so each staged
-// K/V tile serves all G heads.  Per 64-key KV tile:
+// One CTA (256 threads) computes one query tile of 16 R rows (R = 8 at head_dim 128,
+// 4 at 64): 16 R / G consecutive new tokens x the G query heads of kv head `kvh` (rows
+// token-major, heads inner), so each staged K/V tile serves all G heads.  Per 64-key KV
+// tile:
 //   S = Q K^T     thread (ty, tx) = (threadIdx.x / 16, threadIdx.x % 16) computes rows
-//                 4 ty + i and keys tx + 16 j (i, j < 4) from shared memory, float4
-//                 reads (8 reads per 64 FMAs).  Only K rows are padded by 16 bytes: a
-//                 K read touches 16 rows at one column, while Q and P reads are
-//                 broadcasts and V reads cover 16 consecutive pieces of one row, so
-//                 they are conflict-free unpadded (113 KB: two CTAs per SM at D 128)
+//                 R ty + i and keys tx + 16 j (i < R, j < 4) from shared memory, float4
+//                 reads (R + 4 reads per 16 R FMAs).  Only K rows are padded by 16
+//                 bytes: a K read touches 16 rows at one column, while Q and P reads
+//                 are broadcasts and V reads cover 16 consecutive pieces of one row, so
+//                 they are conflict-free unpadded (head_dim 128: 161 KB, one CTA per SM
+//                 with up to 255 registers a thread; head_dim 64: 66 KB, three)
 //   softmax       online, log2 domain; the 16 threads of a half-warp share a row and
 //                 meet by shuffles for its max; each keeps its share of the row sum
-//   O += P V      P through shared memory; the same thread owns rows 4 ty + i and
-//                 columns 4 tx + 64 c of O in registers (12 reads per 128 FMAs)
+//   O += P V      P through shared memory; the same thread owns rows R ty + i and
+//                 columns 4 tx + 64 c of O in registers (R + 2 D / 64 reads per 8 R D / 64
+//                 FMAs per key step)
 // K and V are staged by cp.async (16-byte pieces, zero-filled past the last key the
 // tile needs); the next tile's K loads while P.V runs and its V while S runs.
 #include <cuda_runtime.h>
@@ -31,19 +34,22 @@ namespace pkv {
 
 namespace {
 
-constexpr int kFRows = 64;      // query rows per CTA
 constexpr int kFKeys = 64;      // keys per KV tile
 constexpr int kFThreads = 256;
+// Query rows per thread: 8 at head_dim 128 (a 128-row tile, one CTA per SM), 4 at 64.
+template <int D>
+constexpr int rows_per_thread() { return D == 128 ? 8 : 4; }
 
 template <int D>
 struct FGeom {
+    static constexpr int kRows = 16 * rows_per_thread<D>();   // query rows per CTA
     static constexpr int kKStride = D + 4;         // floats per staged K row (16-byte pad)
     static constexpr int kPStride = kFKeys;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kFRows * D * 4;
+    static constexpr int kOffK = kOffQ + kRows * D * 4;
     static constexpr int kOffV = kOffK + kFKeys * kKStride * 4;
     static constexpr int kOffP = kOffV + kFKeys * D * 4;
-    static constexpr int kBytes = kOffP + kFRows * kPStride * 4;
+    static constexpr int kBytes = kOffP + kRows * kPStride * 4;
     static constexpr int kPieces = D / 4;          // 16-byte pieces per row
 };
 
@@ -88,13 +94,19 @@ PKV_DEVINL void stage_kv(float* dst, const float* pool, const int32_t* bt, int k
     }
 }
 
-// Two CTAs per SM at head_dim 128 (113 KB of shared memory each); three at head_dim 64
-// (66 KB), where the extra warps hide more shared-memory latency than the registers
-// given up for them cost (a few values spill at 80 registers).
+// At head_dim 128 one CTA per SM with 8 query rows a thread: against 4 rows and two
+// CTAs per SM it halves the shared-memory reads per FMA and keeps twice the independent
+// accumulators per thread, which outweighs the halved warp count (15.27 -> 14.23 ms on
+// the prefix-cached prefill batch).  Three CTAs per SM at head_dim 64 (66 KB), where the
+// extra warps hide more shared-memory latency than the registers given up for them
+// cost (a few values spill at 80 registers).
 template <int D, int G>
-__global__ void __launch_bounds__(kFThreads, D == 64 ? 3 : 2)
+__global__ void __launch_bounds__(kFThreads, D == 64 ? 3 : 1)
 prefill_f32_kernel(const PrefillArgs a) {
     using FG = FGeom<D>;
+    constexpr int kFRows = FG::kRows;
+    constexpr int R = rows_per_thread<D>();
+    constexpr int kPvUnroll = D == 128 ? 4 : 2;   // P.V steps of 4 keys unrolled
     constexpr int TOK = kFRows / G;
     constexpr int OC = D / 64;   // float4 column groups of O per thread: 4 tx + 64 c
     extern __shared__ __align__(16) uint8_t smem_f[];
@@ -149,16 +161,16 @@ prefill_f32_kernel(const PrefillArgs a) {
 
     const int tx = threadIdx.x & 15;
     const int ty = threadIdx.x >> 4;
-    int lim[4];   // last key row 4 ty + i sees
+    int lim[R];   // last key row R ty + i sees
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int tok = t0 + (4 * ty + i) / G;
+    for (int i = 0; i < R; ++i) {
+        const int tok = t0 + (R * ty + i) / G;
         lim[i] = tok < n ? c + tok : c + n - 1;
     }
     const float sl2 = a.scale_log2;
-    float m[4], l[4], o[4][OC][4];
+    float m[R], l[R], o[R][OC][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < R; ++i) {
         m[i] = -1.0e30f;   // finite: exp2(m_old - m_new) stays 0 before the first key
         l[i] = 0.f;
 #pragma unroll
@@ -173,22 +185,22 @@ prefill_f32_kernel(const PrefillArgs a) {
         __syncthreads();
 
         // S = Q K^T for rows 4 ty + i, keys tx + 16 j.
-        float s[4][4];
+        float s[R][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < R; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
 #pragma unroll 4
         for (int d = 0; d < D; d += 4) {
-            float4 qv[4], kv[4];
+            float4 qv[R], kv[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                qv[i] = *reinterpret_cast<const float4*>(Qs + (4 * ty + i) * D + d);
+            for (int i = 0; i < R; ++i)
+                qv[i] = *reinterpret_cast<const float4*>(Qs + (R * ty + i) * D + d);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 kv[j] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * j) * FG::kKStride + d);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < R; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     s[i][j] = fmaf(qv[i].x, kv[j].x, s[i][j]);
@@ -198,9 +210,9 @@ prefill_f32_kernel(const PrefillArgs a) {
                 }
         }
         // Online softmax in the log2 domain; the row max over the half-warp.
-        float alpha[4];
+        float alpha[R];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < R; ++i) {
             float mx = -INFINITY;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -218,7 +230,7 @@ prefill_f32_kernel(const PrefillArgs a) {
             for (int j = 0; j < 4; ++j) {
                 const float p = fast_exp2(s[i][j] - m_new);
                 rs += p;
-                Ps[(4 * ty + i) * FG::kPStride + tx + 16 * j] = p;
+                Ps[(R * ty + i) * FG::kPStride + tx + 16 * j] = p;
             }
             l[i] = l[i] * alpha[i] + rs;
         }
@@ -232,17 +244,17 @@ prefill_f32_kernel(const PrefillArgs a) {
 
         // O = alpha O + P V for rows 4 ty + i, columns 4 tx + 64 cc.
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < R; ++i)
 #pragma unroll
             for (int cc = 0; cc < OC; ++cc)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) o[i][cc][e] *= alpha[i];
-#pragma unroll 2
+#pragma unroll kPvUnroll
         for (int k = 0; k < kFKeys; k += 4) {
-            float4 pv[4];
+            float4 pv[R];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                pv[i] = *reinterpret_cast<const float4*>(Ps + (4 * ty + i) * FG::kPStride + k);
+            for (int i = 0; i < R; ++i)
+                pv[i] = *reinterpret_cast<const float4*>(Ps + (R * ty + i) * FG::kPStride + k);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 float4 vv[OC];
@@ -250,7 +262,7 @@ prefill_f32_kernel(const PrefillArgs a) {
                 for (int cc = 0; cc < OC; ++cc)
                     vv[cc] = *reinterpret_cast<const float4*>(Vs + (k + kk) * D + 64 * cc + 4 * tx);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < R; ++i) {
                     const float p = kk == 0 ? pv[i].x : kk == 1 ? pv[i].y : kk == 2 ? pv[i].z : pv[i].w;
 #pragma unroll
                     for (int cc = 0; cc < OC; ++cc) {
@@ -273,11 +285,11 @@ prefill_f32_kernel(const PrefillArgs a) {
     // Row sums over the half-warp, then O / l for the rows of real tokens.
     float* out = static_cast<float*>(a.out);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < R; ++i) {
         float li = l[i];
 #pragma unroll
         for (int off = 1; off < 16; off <<= 1) li += __shfl_xor_sync(0xffffffffu, li, off);
-        const int rho = 4 * ty + i;
+        const int rho = R * ty + i;
         const int tok = t0 + rho / G;
         if (tok >= n) continue;
         const float inv = 1.f / li;
@@ -296,7 +308,7 @@ cudaError_t launch_f32_g(const PrefillArgs& a, cudaStream_t stream) {
     auto kern = prefill_f32_kernel<D, G>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), FG::kBytes);
     if (e != cudaSuccess) return e;
-    constexpr int TOK = kFRows / G;
+    constexpr int TOK = FG::kRows / G;
     dim3 grid((a.max_new + TOK - 1) / TOK, a.num_kv_heads, a.num_reqs);
     return launch_pdl(kern, grid, dim3(kFThreads), FG::kBytes, stream, a);
 }
