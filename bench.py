@@ -1010,11 +1010,15 @@ def main():
     call_bytes = unique_bytes + (append_bytes if fused else 0)
     achieved = call_bytes / (decode_ms * 1e-3) / 1e9
     del workspace, out
+    # The sub-lines and the oracle timings are single-GPU figures: with N replicas they
+    # would repeat the N = 1 line while every GPU is held, so they run at N = 1 only.
+    single = ws == 1
+    cpu_on = single and not args.no_cpu_baseline
     prefill = None
-    if not args.no_prefill:
+    if single and not args.no_prefill:
         prefill = bench_prefill(pkv, dev, args.prefill_steps, stream, args.block_size,
                                 args.prefill_head_dim, args.prefill_dtype, pk,
-                                cpu=not args.no_cpu_baseline, e2e=not args.no_e2e)
+                                cpu=cpu_on, e2e=not args.no_e2e)
         if prefill["dtype"] == "f32":
             # fp32 pools run on the CUDA cores: fp32 FMA peak from the unit counts and the
             # maximum SM clock (152 SMs x 128 FMA a clock x 2 flop x 2.07 GHz).
@@ -1027,14 +1031,12 @@ def main():
                             "frac": prefill["tflops"] / tpeak,
                             "peak_kind": f"{peak_kind} bf16_tflops (burst; kernel timed alone)"})
     long_decode = cascade_line = None
-    if not args.no_long_decode and args.workload != "70b":
+    if single and not args.no_long_decode and args.workload != "70b":
         long_decode = bench_decode_line(pkv, dev, "70b", args.sub_steps, stream, pk,
-                                        cpu=not args.no_cpu_baseline,
-                                        block_size=args.block_size)
-    if not args.no_cascade_line and not (args.workload == "shared" and cascade):
+                                        cpu=cpu_on, block_size=args.block_size)
+    if single and not args.no_cascade_line and not (args.workload == "shared" and cascade):
         cascade_line = bench_decode_line(pkv, dev, "shared", args.sub_steps, stream, pk,
-                                         cascade=True, cpu=not args.no_cpu_baseline,
-                                         block_size=args.block_size)
+                                         cascade=True, cpu=cpu_on, block_size=args.block_size)
     dtype = {torch.bfloat16: "bf16", torch.float32: "f32"}[case.q.dtype]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
@@ -1074,11 +1076,11 @@ def main():
         "prefill": prefill,
         "long_decode": long_decode,
         "shared_prefix_cascade": cascade_line,
-        "prefix_cache": None if args.no_prefix_cache else bench_prefix_cache(pkv),
+        "prefix_cache": None if (args.no_prefix_cache or not single) else bench_prefix_cache(pkv),
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
-    if not args.no_cpu_baseline:
+    if cpu_on:
         line["cpu_baseline"] = cpu_baseline(case, decode_bytes, tokens)
     print(json.dumps(line), flush=True)
     ranks.close()
