@@ -354,7 +354,8 @@ class HostDecodeStep:
     """paged_decode_append_host with every argument bound once, for a loop that runs
     the same step shape over the same buffers (refilling host_in between calls): each
     call is then one ctypes call on pre-converted arguments, about 3 us less host time
-    than the keyword form.  The tensors are held for the object's lifetime."""
+    than the keyword form.  The stream is bound too (stream=None: the current stream
+    at construction).  The tensors are held for the object's lifetime."""
 
     def __init__(self, k_pool, v_pool, host_in, host_out, scale, *, num_seqs, num_q_heads,
                  max_blocks_per_seq, max_context, staging, partition_blocks=0, stream=None):
