@@ -339,28 +339,28 @@ def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf
 
 
 def prefill_e2e(pkv, case, out, max_new, steps, stream, flops):
-    """The prefill step end to end from pinned host memory, per step: the step's inputs
-    (q, the new K/V rows and their slots, the block tables, the requests' cached and new
-    lengths and q offsets) copied to the device, kv_append + paged_prefill, the output
-    copied back, and a synchronise.  Host seconds over `steps` steps."""
+    """The prefill step end to end from pinned host memory through
+    pkv_paged_prefill_append_host, per step: the step's packed inputs (q, the block
+    tables, the requests' cached and new lengths and q offsets, copied to the device;
+    the new K/V rows and their slots, read in place by the append), the output copied
+    back, and a synchronise.  Host seconds over `steps` steps."""
     import torch
-    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "cached_lens",
-             "new_lens", "q_offsets")
-    host = {n: getattr(case, n).cpu().pin_memory() for n in names}
-    devb = {n: torch.empty_like(getattr(case, n)) for n in names}
+    T, Hq, D = case.q.shape
+    R = case.cached_lens.numel()
+    mbs = case.block_tables.shape[1]
+    lay = pkv.prefill_step_layout(case.k_pool, R, T, Hq, mbs)
+    host_in = torch.empty(lay.bytes, dtype=torch.uint8).pin_memory()
+    pkv.pack_prefill_step(host_in, lay, case.q.cpu(), case.block_tables.cpu(),
+                          case.cached_lens.cpu(), case.new_lens.cpu(), case.q_offsets.cpu(),
+                          case.k_new.cpu(), case.v_new.cpu(), case.slot_mapping.cpu())
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    staging = torch.empty(pkv.prefill_host_staging_bytes(case.k_pool, R, T, Hq, mbs),
+                          dtype=torch.uint8, device=case.q.device)
 
     def step():
-        with torch.cuda.stream(stream):
-            for n in names:
-                devb[n].copy_(host[n], non_blocking=True)
-        pkv.kv_append(case.k_pool, case.v_pool, devb["slot_mapping"], devb["k_new"],
-                      devb["v_new"], stream=stream)
-        pkv.paged_prefill(devb["q"], case.k_pool, case.v_pool, devb["block_tables"],
-                          devb["cached_lens"], devb["new_lens"], devb["q_offsets"],
-                          case.scale, max_new=max_new, out=out, stream=stream)
-        with torch.cuda.stream(stream):
-            out_h.copy_(out, non_blocking=True)
+        pkv.paged_prefill_append_host(case.k_pool, case.v_pool, host_in, out_h, case.scale,
+                                      num_reqs=R, total_new=T, max_new=max_new, num_q_heads=Hq,
+                                      max_blocks_per_seq=mbs, staging=staging, stream=stream)
         stream.synchronize()
 
     for _ in range(3):
@@ -372,11 +372,11 @@ def prefill_e2e(pkv, case, out, max_new, steps, stream, flops):
     for _ in range(steps):
         step()
     sec = clock.end() / steps
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    moved = {"h2d_bytes_per_step": lay.bytes, "d2h_bytes_per_step": out_h.numel() * out_h.element_size()}
     return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "ms_per_step": sec * 1e3,
-            "api": "torch H2D copies + kv_append + paged_prefill + torch D2H copy",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
-            "steps": steps}
+            "api": ("pkv_paged_prefill_append_host (pinned buffers: q and the control arrays "
+                    "copied in, the new rows read in place, the output copied back)"),
+            **moved, "steps": steps}
 
 
 def append_sustained(pkv, case, steps, stream, sets=4):

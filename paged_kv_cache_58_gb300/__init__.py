@@ -37,6 +37,16 @@ class PoolDesc(ctypes.Structure):
                 ("dtype", ctypes.c_int32)]
 
 
+class PrefillLayout(ctypes.Structure):
+    """Byte offsets of one prefill step's inputs in a packed host buffer: the part copied
+    to the device (q and the control arrays, `copied_bytes`), then the new rows."""
+    _fields_ = [("q", ctypes.c_uint64), ("block_tables", ctypes.c_uint64),
+                ("cached_lens", ctypes.c_uint64), ("new_lens", ctypes.c_uint64),
+                ("q_offsets", ctypes.c_uint64), ("copied_bytes", ctypes.c_uint64),
+                ("k_new", ctypes.c_uint64), ("v_new", ctypes.c_uint64),
+                ("slot_mapping", ctypes.c_uint64), ("bytes", ctypes.c_uint64)]
+
+
 class StepLayout(ctypes.Structure):
     """Byte offsets of one decode step's inputs in a packed host buffer (and its size)."""
     _fields_ = [("q", ctypes.c_uint64), ("k_new", ctypes.c_uint64), ("v_new", ctypes.c_uint64),
@@ -87,6 +97,13 @@ def _load():
                                            P(StepLayout)]
     lib.pkv_paged_decode_append_host_staging_bytes.restype = sz
     lib.pkv_paged_decode_append_host_staging_bytes.argtypes = [P(PoolDesc)] + [ctypes.c_int] * 5
+    lib.pkv_prefill_step_layout.restype = ctypes.c_int
+    lib.pkv_prefill_step_layout.argtypes = [P(PoolDesc)] + [ctypes.c_int] * 4 + [P(PrefillLayout)]
+    lib.pkv_paged_prefill_append_host_staging_bytes.restype = sz
+    lib.pkv_paged_prefill_append_host_staging_bytes.argtypes = [P(PoolDesc)] + [ctypes.c_int] * 4
+    lib.pkv_paged_prefill_append_host.restype = ctypes.c_int
+    lib.pkv_paged_prefill_append_host.argtypes = [P(PoolDesc), vp, vp, vp, vp] + \
+        [ctypes.c_int] * 5 + [f32, vp, sz, vp]
     lib.pkv_paged_decode_append_host.restype = ctypes.c_int
     lib.pkv_paged_decode_append_host.argtypes = [P(PoolDesc), vp, vp, vp, vp, ctypes.c_int,
                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, f32,
@@ -380,6 +397,52 @@ class HostDecodeStep:
         if st != 0:
             raise PkvError("pkv_paged_decode_append_host", st)
         return self.host_out
+
+
+def prefill_step_layout(k_pool, num_reqs, total_new, num_q_heads,
+                        max_blocks_per_seq) -> PrefillLayout:
+    """Packed host-buffer layout of one prefill step's inputs (pkv_prefill_step_layout)."""
+    lay = PrefillLayout()
+    _check("pkv_prefill_step_layout",
+           _load().pkv_prefill_step_layout(ctypes.byref(pool_desc(k_pool)), num_reqs, total_new,
+                                           num_q_heads, max_blocks_per_seq, ctypes.byref(lay)))
+    return lay
+
+
+def pack_prefill_step(host_in, layout, q, block_tables, cached_lens, new_lens, q_offsets,
+                      k_new, v_new, slot_mapping):
+    """Write one prefill step's inputs (CPU tensors) into the packed host buffer
+    `host_in` (uint8)."""
+    for off, t in ((layout.q, q), (layout.block_tables, block_tables),
+                   (layout.cached_lens, cached_lens), (layout.new_lens, new_lens),
+                   (layout.q_offsets, q_offsets), (layout.k_new, k_new),
+                   (layout.v_new, v_new), (layout.slot_mapping, slot_mapping)):
+        b = t.contiguous().view(torch.uint8).reshape(-1)
+        host_in[off:off + b.numel()].copy_(b)
+
+
+def prefill_host_staging_bytes(k_pool, num_reqs, total_new, num_q_heads, max_blocks_per_seq):
+    return int(_load().pkv_paged_prefill_append_host_staging_bytes(
+        ctypes.byref(pool_desc(k_pool)), num_reqs, total_new, num_q_heads, max_blocks_per_seq))
+
+
+def paged_prefill_append_host(k_pool, v_pool, host_in, host_out, scale, *, num_reqs, total_new,
+                              max_new, num_q_heads, max_blocks_per_seq, staging, stream=None):
+    """One prefill step from host memory: host_in (uint8, packed as prefill_step_layout)
+    -> kv_append of the new rows + paged_prefill -> host_out ([total_new, Hq, D]).  q and
+    the control arrays are copied to `staging`, a pinned host_in's new rows are read in
+    place, and the output is copied back.  Queued on the stream; host_out is complete
+    after a synchronise."""
+    if host_in.is_cuda or host_out.is_cuda:
+        raise ValueError("host_in and host_out must be host tensors")
+    st = _load().pkv_paged_prefill_append_host(
+        ctypes.byref(pool_desc(k_pool)), _dev(k_pool, "k_pool"),
+        _dev(v_pool, "v_pool", k_pool.dtype), host_in.data_ptr(), host_out.data_ptr(),
+        int(num_reqs), int(total_new), int(max_new), int(num_q_heads), int(max_blocks_per_seq),
+        float(scale), _dev(staging, "staging"), staging.numel() * staging.element_size(),
+        _stream(stream))
+    _check("pkv_paged_prefill_append_host", st)
+    return host_out
 
 
 def cascade_workspace_bytes(num_seqs, num_q_heads, head_dim, prefix_len, max_context,

@@ -139,3 +139,61 @@ def test_prefill_many_requests_both_schedules(pkv, oracle_mod, num_reqs):
     case = custom_case(32, 8, cached, new, seed=num_reqs, num_blocks=4096)
     ref, _, _ = oracle_prefill_case(oracle_mod, case)
     check_attention(run_prefill(pkv, case), ref, single_p=case_single_p(case))
+
+
+def host_prefill_step(pkv, case, mode):
+    """pkv_paged_prefill_append_host over `case`, host buffers pinned, pageable or pinned
+    but off a 16-byte boundary; returns the host output."""
+    T, Hq, D = case.q.shape
+    R = case.cached_lens.numel()
+    mbs = case.block_tables.shape[1]
+    lay = pkv.prefill_step_layout(case.k_pool, R, T, Hq, mbs)
+    esz = case.q.element_size()
+    if mode == "pinned_unaligned":
+        host_in = torch.empty(lay.bytes + 16, dtype=torch.uint8).pin_memory()[8:8 + lay.bytes]
+        raw = torch.empty((T * Hq * D + 16) * esz, dtype=torch.uint8).pin_memory()
+        host_out = raw[esz:esz + T * Hq * D * esz].view(case.q.dtype).view(T, Hq, D)
+    else:
+        host_in = torch.empty(lay.bytes, dtype=torch.uint8)
+        host_out = torch.empty((T, Hq, D), dtype=case.q.dtype)
+        if mode == "pinned":
+            host_in, host_out = host_in.pin_memory(), host_out.pin_memory()
+    host_out.fill_(float("nan"))
+    pkv.pack_prefill_step(host_in, lay, case.q.cpu(), case.block_tables.cpu(),
+                          case.cached_lens.cpu(), case.new_lens.cpu(), case.q_offsets.cpu(),
+                          case.k_new.cpu(), case.v_new.cpu(), case.slot_mapping.cpu())
+    staging = torch.empty(pkv.prefill_host_staging_bytes(case.k_pool, R, T, Hq, mbs),
+                          dtype=torch.uint8, device="cuda")
+    pkv.paged_prefill_append_host(case.k_pool, case.v_pool, host_in, host_out, case.scale,
+                                  num_reqs=R, total_new=T, max_new=int(case.new_lens.max()),
+                                  num_q_heads=Hq, max_blocks_per_seq=mbs, staging=staging)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    return host_out
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("mode", ["pinned", "pageable", "pinned_unaligned"])
+def test_prefill_host_step_matches_device_calls(pkv, mode, dtype):
+    """pkv_paged_prefill_append_host (q and the control arrays copied, the new rows read
+    in place when pinned, the output copied back) gives the output bits and pools of
+    kv_append + paged_prefill on device buffers, on bf16 (tensor cores) and fp32 (CUDA
+    cores) pools."""
+    a = custom_case(32, 8, [0, 100, 1000, 16, 33], [37, 64, 300, 1, 128], seed=5, dtype=dtype)
+    b = custom_case(32, 8, [0, 100, 1000, 16, 33], [37, 64, 300, 1, 128], seed=5, dtype=dtype)
+    ref = run_prefill(pkv, b)
+    out = host_prefill_step(pkv, a, mode)
+    assert torch.equal(out.view(torch.uint8), ref.cpu().view(torch.uint8))
+    assert torch.equal(a.k_pool.view(torch.uint8), b.k_pool.view(torch.uint8))
+    assert torch.equal(a.v_pool.view(torch.uint8), b.v_pool.view(torch.uint8))
+
+
+def test_prefill_host_step_published_batch(pkv):
+    """The prefix-cached prefill batch (16 x 512 new tokens) through the host step with
+    pinned buffers: the device calls' output bits."""
+    a = synth.build_case("prefill", "cuda")
+    b = synth.build_case("prefill", "cuda")
+    ref = run_prefill(pkv, b)
+    out = host_prefill_step(pkv, a, "pinned")
+    assert torch.equal(out.view(torch.uint8), ref.cpu().view(torch.uint8))
+

@@ -228,6 +228,29 @@ def test_decode_step_layout(pkv):
                                             ctypes.byref(lay)) == 1
 
 
+def test_prefill_step_layout(pkv):
+    """Packed host layout of a prefill step: the copied part (q, tables, lengths,
+    offsets) first, then the new rows and slots, 256-byte aligned; the staging adds the
+    output."""
+    d = pkv.PoolDesc(32768, 16, 8, 128, 1)
+    lay = pkv.PrefillLayout()
+    assert pkv.lib().pkv_prefill_step_layout(ctypes.byref(d), 16, 8192, 32, 513,
+                                             ctypes.byref(lay)) == 0
+    offs = [lay.q, lay.block_tables, lay.cached_lens, lay.new_lens, lay.q_offsets,
+            lay.copied_bytes, lay.v_new, lay.slot_mapping, lay.bytes]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert lay.q == 0 and lay.block_tables >= 8192 * 32 * 128 * 2
+    assert lay.cached_lens - lay.block_tables >= 16 * 513 * 4
+    assert lay.copied_bytes - lay.q_offsets >= 17 * 4 and lay.k_new == lay.copied_bytes
+    assert lay.v_new - lay.k_new >= 8192 * 8 * 128 * 2
+    assert lay.bytes - lay.slot_mapping >= 8192 * 8
+    staging = pkv.lib().pkv_paged_prefill_append_host_staging_bytes(ctypes.byref(d), 16, 8192,
+                                                                    32, 513)
+    assert staging == lay.bytes + 8192 * 32 * 128 * 2
+    assert pkv.lib().pkv_prefill_step_layout(ctypes.byref(d), -1, 8192, 32, 513,
+                                             ctypes.byref(lay)) == 1
+
+
 def test_auto_partition_is_a_multiple_of_four_chunks():
     """The library's split-KV partition size, in 16-token chunks, is a multiple of 4 (one
     chunk per warp per step, and whole 32-token blocks) and at least 8, over a grid of
