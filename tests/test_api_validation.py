@@ -132,3 +132,37 @@ def test_host_step_checks(pkv):
     assert h(hout=None) == INVALID
     assert h(stg=0x100010) == INVALID     # staging must be 256-byte aligned
     assert h(stgb=64) == NOMEM
+
+
+def test_prefill_host_step_checks(pkv):
+    """Argument errors of the host-buffer prefill step are returned before any CUDA call:
+    sizes, null buffers, staging alignment and size, and q_offsets read from host_in that
+    are not the prefix sum ending at total_new."""
+    import numpy as np
+    lib = pkv.lib()
+    d = desc(pkv)
+    R, T, Hq, mbs = 2, 10, 32, 4
+    lay = pkv.PrefillLayout()
+    assert lib.pkv_prefill_step_layout(ctypes.byref(d), R, T, Hq, mbs, ctypes.byref(lay)) == OK
+    host = np.zeros(lay.bytes, dtype=np.uint8)
+    qo = host[lay.q_offsets:lay.q_offsets + 4 * (R + 1)].view(np.int32)
+    need = lib.pkv_paged_prefill_append_host_staging_bytes(ctypes.byref(d), R, T, Hq, mbs)
+    ps = lib.pkv_paged_prefill_append_host
+
+    def h(hin=None, hout=A, stg=0x100000, stgb=None, R=R, T=T):
+        hin = host.ctypes.data if hin is None else hin
+        return ps(ctypes.byref(d), A, A, hin, hout, R, T, 8, Hq, mbs, 0.1, stg,
+                  need if stgb is None else stgb, None)
+
+    qo[:] = [0, 4, 11]                     # ends past total_new
+    assert h() == INVALID
+    qo[:] = [0, 6, 4]                      # decreasing
+    assert h() == INVALID
+    qo[:] = [1, 4, 10]                     # does not start at 0
+    assert h() == INVALID
+    assert h(R=0) == OK and h(T=0) == OK
+    assert h(hout=None) == INVALID
+    assert h(stg=0x100010) == INVALID      # staging must be 256-byte aligned
+    assert h(stgb=64) == NOMEM
+    assert lib.pkv_prefill_step_layout(ctypes.byref(d), R, -1, Hq, mbs, ctypes.byref(lay)) == INVALID
+
