@@ -341,9 +341,9 @@ def bench_prefill(pkv, dev, steps, stream, block_size=0, head_dim=128, dtype="bf
 def prefill_e2e(pkv, case, out, max_new, steps, stream, flops):
     """The prefill step end to end from pinned host memory through
     pkv_paged_prefill_append_host, per step: the step's packed inputs (q, the block
-    tables, the requests' cached and new lengths and q offsets, copied to the device;
-    the new K/V rows and their slots, read in place by the append), the output copied
-    back, and a synchronise.  Host seconds over `steps` steps."""
+    tables, the requests' cached and new lengths and q offsets, the new K/V rows and
+    their slots) copied in, the output copied back, and a synchronise.  Host seconds
+    over `steps` steps."""
     import torch
     T, Hq, D = case.q.shape
     R = case.cached_lens.numel()
@@ -374,8 +374,8 @@ def prefill_e2e(pkv, case, out, max_new, steps, stream, flops):
     sec = clock.end() / steps
     moved = {"h2d_bytes_per_step": lay.bytes, "d2h_bytes_per_step": out_h.numel() * out_h.element_size()}
     return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "ms_per_step": sec * 1e3,
-            "api": ("pkv_paged_prefill_append_host (pinned buffers: q and the control arrays "
-                    "copied in, the new rows read in place, the output copied back)"),
+            "api": ("pkv_paged_prefill_append_host (pinned buffers; copies in and out "
+                    "pipelined with the kernels over 4 request chunks)"),
             **moved, "steps": steps}
 
 

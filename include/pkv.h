@@ -303,7 +303,8 @@ pkv_status pkv_paged_prefill(const pkv_pool_desc* pool, void* out, const void* q
  * layout the device calls take: first the part copied to the device (q, which the
  * tensor-core prefill loads by TMA, and the block tables, cached_lens, new_lens and
  * q_offsets: `copied_bytes` bytes), then the new rows k_new, v_new ([total_new]
- * [num_kv_heads][head_dim]) and slot_mapping (int64 [total_new]).
+ * [num_kv_heads][head_dim]) and slot_mapping (int64 [total_new]).  (All of it is copied
+ * to the device; `copied_bytes` marks where the per-request arrays end.)
  *   layout  out: byte offsets of the eight arrays, copied_bytes and the total size.
  * Returns PKV_ERR_INVALID for bad sizes. */
 typedef struct pkv_prefill_layout {
@@ -320,20 +321,18 @@ size_t pkv_paged_prefill_append_host_staging_bytes(const pkv_pool_desc* pool, in
                                                    int total_new, int num_q_heads,
                                                    int max_blocks_per_seq);
 
-/* One prefill step from host memory, queued on `stream`: the copied part of host_in
- * goes to `staging`; pkv_kv_append stores the new rows; pkv_paged_prefill writes the
- * output ([total_new][num_q_heads][head_dim], pool dtype) into staging, which is copied
- * back to host_out.  When host_in is page-locked memory mapped into the device's address
- * space (cudaHostAlloc, cudaMallocHost, cudaHostRegister under unified addressing) and
- * 16-byte aligned, the append kernel reads the new rows and slots in place over the host
- * link; otherwise they are copied too.  The call reads q_offsets from host_in (it must
- * be the exclusive prefix sum of new_lens, ending at total_new: PKV_ERR_INVALID
- * otherwise) and splits the requests into up to 4 chunks of about equal new rows: a
- * chunk's q is copied in on a library-owned stream while the previous chunk's append
- * and prefill run on `stream` and the one before's output is copied back on a second
- * library-owned stream; every return, errors included, first makes `stream` wait for
- * both.  host_out is complete once `stream` has been synchronised, and host_in must
- * stay unchanged until then.
+/* One prefill step from host memory, queued on `stream`: host_in goes to `staging`,
+ * pkv_kv_append stores the new rows, pkv_paged_prefill writes the output
+ * ([total_new][num_q_heads][head_dim], pool dtype) into staging, which is copied back
+ * to host_out.  Host buffers should be page-locked for the copies to run
+ * asynchronously.  The call reads q_offsets from host_in (it must be the exclusive
+ * prefix sum of new_lens, ending at total_new: PKV_ERR_INVALID otherwise) and splits the
+ * requests into up to 4 chunks of about equal new rows: a chunk's q, new rows and slots
+ * are copied in on a library-owned stream while the previous chunk's append and prefill
+ * run on `stream` and the one before's output is copied back on a second library-owned
+ * stream; every return, errors included, first makes `stream` wait for both.  host_out
+ * is complete once `stream` has been synchronised, and host_in must stay unchanged until
+ * then.
  *   staging  device, >= pkv_paged_prefill_append_host_staging_bytes(...) bytes, 256-byte
  *            aligned; contents need no initialisation and are clobbered.
  * Argument errors as pkv_kv_append and pkv_paged_prefill; PKV_ERR_NOMEM if staging is

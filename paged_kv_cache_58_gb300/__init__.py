@@ -429,10 +429,9 @@ def prefill_host_staging_bytes(k_pool, num_reqs, total_new, num_q_heads, max_blo
 def paged_prefill_append_host(k_pool, v_pool, host_in, host_out, scale, *, num_reqs, total_new,
                               max_new, num_q_heads, max_blocks_per_seq, staging, stream=None):
     """One prefill step from host memory: host_in (uint8, packed as prefill_step_layout)
-    -> kv_append of the new rows + paged_prefill -> host_out ([total_new, Hq, D]).  q and
-    the control arrays are copied to `staging`, a pinned host_in's new rows are read in
-    place, and the output is copied back.  Queued on the stream; host_out is complete
-    after a synchronise."""
+    -> kv_append of the new rows + paged_prefill -> host_out ([total_new, Hq, D]),
+    through `staging`, with the copies pipelined against the kernels over request chunks.
+    Queued on the stream; host_out is complete after a synchronise."""
     if host_in.is_cuda or host_out.is_cuda:
         raise ValueError("host_in and host_out must be host tensors")
     st = _load().pkv_paged_prefill_append_host(

@@ -846,13 +846,12 @@ pkv_status pkv_paged_prefill_append_host(const pkv_pool_desc* pool, void* k_pool
     const uint64_t qrow = static_cast<uint64_t>(num_q_heads) * pool->head_dim * esz;
     const uint64_t kvrow = static_cast<uint64_t>(pool->num_kv_heads) * pool->head_dim * esz;
     const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
-    // q and the control arrays always go to the device (the prefill loads q by TMA); the
-    // new rows are read in place from mapped (page-locked) host memory, else copied too.
-    // The output goes through staging and one copy back per chunk: stored in place over
-    // the host link, the prefill's output tiles held the kernel up (1.23 -> 1.87 ms a step
-    // on the 16 x 512-token batch).
-    const char* rows = static_cast<const char*>(mapped_host_ptr(host_in));
-    if (!aligned16(rows)) rows = nullptr;
+    // Every input goes to the device by copy (the prefill loads q by TMA) and the output
+    // comes back by copy, chunk by chunk, on two library streams beside the kernels.  On
+    // the 16 x 512-token batch the link moves about 200 GB/s each way, whether copy
+    // engines or SMs drive it; read in place by the append kernel, the new rows cost
+    // more on the kernels' stream than their copy does beside it, and stored in place the
+    // prefill's output tiles held the kernel up (1.23 -> 1.87 ms a step unchunked).
     // Requests in up to kChunks chunks of about equal new rows: chunk c's query rows are
     // copied in on one copy stream while chunk c - 1's append and prefill run on `stream`
     // and chunk c - 2's output is copied back on the other.
@@ -901,22 +900,20 @@ pkv_status pkv_paged_prefill_append_host(const pkv_pool_desc* pool, void* k_pool
             }
         }
     } rejoin{cin, cout, st_, &ev};
-    // the control arrays (and, from pageable memory, the new rows), then chunk by chunk q
+    // the control arrays, then chunk by chunk q, the new rows and their slots
     if (cudaMemcpyAsync(dev + l.block_tables, hin + l.block_tables,
                         l.copied_bytes - l.block_tables, cudaMemcpyHostToDevice, cin) != cudaSuccess)
         return PKV_ERR_CUDA;
-    if (!rows) {
-        if (cudaMemcpyAsync(dev + l.k_new, hin + l.k_new, l.bytes - l.k_new,
-                            cudaMemcpyHostToDevice, cin) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        rows = dev;
-    }
     cudaEvent_t in_done[kChunks];
     for (int c = 0; c < nch; ++c) {
         const uint64_t t0 = qoff[bounds[c]], t1 = qoff[bounds[c + 1]];
-        if (t1 > t0 && cudaMemcpyAsync(dev + l.q + t0 * qrow, hin + l.q + t0 * qrow,
-                                       (t1 - t0) * qrow, cudaMemcpyHostToDevice, cin) != cudaSuccess)
-            return PKV_ERR_CUDA;
+        const struct { uint64_t off, row; } parts[4] = {
+            {l.q, qrow}, {l.k_new, kvrow}, {l.v_new, kvrow}, {l.slot_mapping, sizeof(int64_t)}};
+        for (const auto& pt : parts)
+            if (t1 > t0 && cudaMemcpyAsync(dev + pt.off + t0 * pt.row, hin + pt.off + t0 * pt.row,
+                                           (t1 - t0) * pt.row, cudaMemcpyHostToDevice,
+                                           cin) != cudaSuccess)
+                return PKV_ERR_CUDA;
         in_done[c] = ev.make();
         if (!in_done[c] || cudaEventRecord(in_done[c], cin) != cudaSuccess) return PKV_ERR_CUDA;
     }
@@ -924,6 +921,7 @@ pkv_status pkv_paged_prefill_append_host(const pkv_pool_desc* pool, void* k_pool
     const int32_t* dcl = reinterpret_cast<const int32_t*>(dev + l.cached_lens);
     const int32_t* dnl = reinterpret_cast<const int32_t*>(dev + l.new_lens);
     const int32_t* dqo = reinterpret_cast<const int32_t*>(dev + l.q_offsets);
+    const char* rows = dev;
     const int64_t* slots = reinterpret_cast<const int64_t*>(rows + l.slot_mapping);
     for (int c = 0; c < nch; ++c) {
         const int r0 = bounds[c], r1 = bounds[c + 1];

@@ -175,10 +175,10 @@ def host_prefill_step(pkv, case, mode):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("mode", ["pinned", "pageable", "pinned_unaligned"])
 def test_prefill_host_step_matches_device_calls(pkv, mode, dtype):
-    """pkv_paged_prefill_append_host (q and the control arrays copied, the new rows read
-    in place when pinned, the output copied back) gives the output bits and pools of
-    kv_append + paged_prefill on device buffers, on bf16 (tensor cores) and fp32 (CUDA
-    cores) pools."""
+    """pkv_paged_prefill_append_host (inputs copied in and the output copied back, in
+    request chunks beside the kernels) gives the output bits and pools of kv_append +
+    paged_prefill on device buffers, on bf16 (tensor cores) and fp32 (CUDA cores) pools,
+    from pinned, pageable and misaligned pinned host buffers."""
     a = custom_case(32, 8, [0, 100, 1000, 16, 33], [37, 64, 300, 1, 128], seed=5, dtype=dtype)
     b = custom_case(32, 8, [0, 100, 1000, 16, 33], [37, 64, 300, 1, 128], seed=5, dtype=dtype)
     ref = run_prefill(pkv, b)
