@@ -1,8 +1,9 @@
-"""Stream capture: a decode step (kv_append + paged_decode, or the fused call) and a
-cascade decode can be recorded into a CUDA graph and replayed -- the calls allocate
-nothing, read nothing back to the host and never synchronise -- and a replay gives the
-same bits as the eager calls.
-The cascade's fork onto the library's side stream becomes part of the graph."""
+"""Stream capture: a decode step (kv_append + paged_decode, or the fused call), a
+cascade decode and the host-buffer decode and prefill steps (pinned buffers) can be
+recorded into a CUDA graph and replayed -- the calls allocate nothing and never
+synchronise -- and a replay gives the same bits as the eager calls.
+The forks onto the library's own streams (the cascade's prefix pass, the prefill
+step's copies) become part of the graph."""
 import dataclasses
 
 import pytest
@@ -199,3 +200,59 @@ def test_cascade_error_after_fork_leaves_capture_joined(pkv, monkeypatch):
     torch.cuda.synchronize()
     assert pkv.read_device_status() == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_host_steps_graph_replay(pkv):
+    """The host-buffer decode step (kernels reading and writing pinned memory in place)
+    and the host-buffer prefill step (chunked copies on the library's copy streams,
+    joined back) captured and replayed: the eager calls' host output bits."""
+    # decode step
+    a = synth.build_case(dataclasses.replace(synth.WORKLOADS["8b"], num_seqs=16,
+                                             num_blocks=4096), "cuda", seed=33)
+    S, Hq, D = a.q.shape
+    mbs = a.block_tables.shape[1]
+    lay = pkv.decode_step_layout(a.k_pool, S, Hq, mbs)
+    hin = torch.empty(lay.bytes, dtype=torch.uint8).pin_memory()
+    pkv.pack_decode_step(hin, lay, a.q.cpu(), a.k_new.cpu(), a.v_new.cpu(),
+                         a.block_tables.cpu(), a.context_lens.cpu())
+    stg = torch.empty(pkv.decode_host_staging_bytes(a.k_pool, S, Hq, mbs, a.max_context),
+                      dtype=torch.uint8, device="cuda")
+    ref = torch.empty((S, Hq, D), dtype=a.q.dtype).pin_memory()
+    got = torch.full((S, Hq, D), float("nan"), dtype=a.q.dtype).pin_memory()
+    kw = dict(num_seqs=S, num_q_heads=Hq, max_blocks_per_seq=mbs, max_context=a.max_context,
+              staging=stg)
+    pkv.paged_decode_append_host(a.k_pool, a.v_pool, hin, ref, a.scale, **kw)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    g = capture(lambda: pkv.paged_decode_append_host(a.k_pool, a.v_pool, hin, got, a.scale,
+                                                     **kw))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.uint8), ref.view(torch.uint8))
+    # prefill step
+    b = synth.build_case(dataclasses.replace(synth.WORKLOADS["prefill"], num_seqs=6,
+                                             num_blocks=8192), "cuda", seed=35)
+    T, Hq, D = b.q.shape
+    R = b.cached_lens.numel()
+    mbs = b.block_tables.shape[1]
+    play = pkv.prefill_step_layout(b.k_pool, R, T, Hq, mbs)
+    phin = torch.empty(play.bytes, dtype=torch.uint8).pin_memory()
+    pkv.pack_prefill_step(phin, play, b.q.cpu(), b.block_tables.cpu(), b.cached_lens.cpu(),
+                          b.new_lens.cpu(), b.q_offsets.cpu(), b.k_new.cpu(), b.v_new.cpu(),
+                          b.slot_mapping.cpu())
+    pstg = torch.empty(pkv.prefill_host_staging_bytes(b.k_pool, R, T, Hq, mbs),
+                       dtype=torch.uint8, device="cuda")
+    pref = torch.empty((T, Hq, D), dtype=b.q.dtype).pin_memory()
+    pgot = torch.full((T, Hq, D), float("nan"), dtype=b.q.dtype).pin_memory()
+    pkw = dict(num_reqs=R, total_new=T, max_new=int(b.new_lens.max()), num_q_heads=Hq,
+               max_blocks_per_seq=mbs, staging=pstg)
+    pkv.paged_prefill_append_host(b.k_pool, b.v_pool, phin, pref, b.scale, **pkw)
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    g2 = capture(lambda: pkv.paged_prefill_append_host(b.k_pool, b.v_pool, phin, pgot, b.scale,
+                                                       **pkw))
+    g2.replay()
+    torch.cuda.synchronize()
+    assert pkv.read_device_status() == 0
+    assert torch.equal(pgot.view(torch.uint8), pref.view(torch.uint8))
+
